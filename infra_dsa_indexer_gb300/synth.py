@@ -1,0 +1,243 @@
+"""Seeded synthetic inputs for the lightning-indexer MQA logits.
+
+This module makes input bytes and nothing else: Gaussian draws, their
+quantisation into the input formats (BF16, E4M3, MXFP8 = E4M3 + E8M0 per
+32-element block, MXFP4 = E2M1 + E8M0) and the per-row key windows. It holds
+none of the logits arithmetic; the CUDA path and the float64 oracle both
+consume exactly the bytes made here.
+
+Quantisation recipe (it shapes the inputs only, never parity):
+  * BF16: round-to-nearest-even of the float32 draw.
+  * FP8 per-token: per key row, scale = amax/448 (amax 0 -> 1), element =
+    e4m3(x/scale). Q gets one scale per query row (all heads), folded into W.
+  * MX (OCP Microscaling v1.0): per 32-element block, shared exponent
+    X = floor(log2(amax)) - emax_elem (emax 8 for E4M3, 2 for E2M1), stored as
+    the E8M0 byte X+127; element = x / 2^X rounded to nearest-even and
+    saturated to the element format's largest finite value.
+  * E2M1 packs two elements per byte, the even element in the low nibble.
+
+Random draws use numpy's PCG64 so the same seed gives the same bytes on every
+machine.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import torch
+
+FMT_BF16, FMT_E4M3, FMT_MXFP8, FMT_MXFP4 = 0, 1, 2, 3
+W_F32, W_BF16 = 0, 1
+FMT_NAMES = {FMT_BF16: "bf16", FMT_E4M3: "e4m3", FMT_MXFP8: "mxfp8", FMT_MXFP4: "mxfp4"}
+
+E4M3_MAX = 448.0
+
+
+@dataclasses.dataclass
+class Case:
+    """One problem instance: raw input bytes plus its shape and scalars."""
+    name: str
+    fmt: int
+    B: int
+    S: int
+    N: int
+    H: int
+    D: int
+    sm_scale: float               # exactly representable in float32
+    q: np.ndarray                 # [B,S,H,row]  uint16 (bf16) / uint8
+    k: np.ndarray                 # [B,N,row]
+    w: np.ndarray                 # [B,S,H] float32, or uint16 bf16 codes
+    w_fmt: int
+    ks: np.ndarray                # [B,S] int32
+    ke: np.ndarray                # [B,S] int32
+    q_sf: np.ndarray | None = None  # [B,S,H,D/32] uint8 E8M0
+    k_sf: np.ndarray | None = None  # [B,N,D/32] uint8 E8M0
+    k_tok: np.ndarray | None = None  # [B,N] float32 per-token K scale
+    clean: bool = True
+
+    def in_window_pairs(self) -> int:
+        lo = np.clip(self.ks.astype(np.int64), 0, self.N)
+        hi = np.clip(self.ke.astype(np.int64), 0, self.N)
+        return int(np.maximum(hi - lo, 0).sum())
+
+    def in_window_flops(self) -> float:
+        return 2.0 * self.H * self.D * self.in_window_pairs()
+
+
+# ----------------------------------------------------------------------------
+# element encoders
+# ----------------------------------------------------------------------------
+
+def to_bf16_codes(x: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def to_e4m3_codes(x: np.ndarray) -> np.ndarray:
+    """Round-to-nearest-even into OCP E4M3, saturating at +-448."""
+    x = np.clip(np.asarray(x, dtype=np.float32), -E4M3_MAX, E4M3_MAX)
+    t = torch.from_numpy(np.ascontiguousarray(x))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+# E2M1 magnitudes by code: 0, 0.5, 1, 1.5, 2, 3, 4, 6. Midpoints between
+# neighbours, and whether a value exactly on a midpoint rounds up (to the
+# even code above) or stays on the even code below.
+_E2M1_MIDPOINTS = ((0.25, False), (0.75, True), (1.25, False), (1.75, True),
+                   (2.5, False), (3.5, True), (5.0, False))
+
+
+def to_e2m1_codes(x: np.ndarray) -> np.ndarray:
+    """Round-to-nearest-even into E2M1 (one code per uint8), saturating at 6."""
+    x = np.asarray(x, dtype=np.float32)
+    ax = np.abs(x)
+    code = np.zeros(x.shape, dtype=np.uint8)
+    for mid, tie_up in _E2M1_MIDPOINTS:
+        code += (ax >= mid) if tie_up else (ax > mid)
+    code |= (np.signbit(x) & (code != 0)).astype(np.uint8) << 3
+    return code
+
+
+def pack_e2m1(codes: np.ndarray) -> np.ndarray:
+    """[..., D] codes -> [..., D/2] bytes, element 2k in the low nibble."""
+    lo = codes[..., 0::2]
+    hi = codes[..., 1::2]
+    return (lo | (hi << 4)).astype(np.uint8)
+
+
+def mx_quantize(x: np.ndarray, elem: str):
+    """OCP MX quantisation along the last axis (blocks of 32).
+
+    Returns (element codes [..., D] for e4m3 / packed [..., D/2] for e2m1,
+    E8M0 scale bytes [..., D/32])."""
+    emax = {"e4m3": 8, "e2m1": 2}[elem]
+    D = x.shape[-1]
+    assert D % 32 == 0
+    xb = x.reshape(*x.shape[:-1], D // 32, 32)
+    amax = np.abs(xb).max(axis=-1)
+    _, e = np.frexp(amax)                     # amax = m * 2^e, m in [0.5, 1)
+    X = (e.astype(np.int32) - 1) - emax      # floor(log2(amax)) - emax
+    X = np.where(amax > 0, X, 0)
+    X = np.clip(X, -127, 127)
+    sf = (X + 127).astype(np.uint8)
+    scaled = xb / np.exp2(X.astype(np.float32))[..., None]
+    scaled = scaled.reshape(x.shape)
+    if elem == "e4m3":
+        return to_e4m3_codes(scaled), sf
+    return pack_e2m1(to_e2m1_codes(scaled)), sf
+
+
+# ----------------------------------------------------------------------------
+# windows
+# ----------------------------------------------------------------------------
+
+def causal_windows(B, S, N, offset):
+    """Row i sees [0, offset + i)."""
+    ke = (np.arange(S, dtype=np.int64) + offset)
+    ke = np.broadcast_to(ke, (B, S)).astype(np.int32)
+    return np.zeros((B, S), dtype=np.int32), np.ascontiguousarray(ke)
+
+
+FORCED_EMPTY_ROWS = (0, 1, 127, 128, 4095, 4096, 8190, 8191)
+
+
+def irregular_windows(rng, B, S, N, forced_empty=FORCED_EMPTY_ROWS):
+    """ks ~ U[0, N/2), length ~ U[0, N/2] inclusive, ke = ks + length; rows in
+    `forced_empty` (those below S) get length 0."""
+    ks = rng.integers(0, N // 2, size=(B, S), dtype=np.int64)
+    ln = rng.integers(0, N // 2 + 1, size=(B, S), dtype=np.int64)
+    for r in forced_empty:
+        if r < S:
+            ln[:, r] = 0
+    return ks.astype(np.int32), (ks + ln).astype(np.int32)
+
+
+# ----------------------------------------------------------------------------
+# case builder
+# ----------------------------------------------------------------------------
+
+def make_case(fmt, B, S, N, H=64, D=128, *, seed=0, windows="full",
+              w_fmt=W_F32, w_std=1.0 / 8.0, sm_scale=None, ks=None, ke=None,
+              zero=False, name=None, mx_unit_scales=False) -> Case:
+    """Draw Q, K ~ N(0,1), W ~ N(0, w_std^2), quantise to `fmt`.
+
+    windows: "full" ([0,N)), "causal" ([0, N-S+i+1)), "causal_excl"
+    ([0, N-S+i)), "irregular" (random, see irregular_windows), or give ks/ke.
+    zero=True makes all-zero Q/K/W (MX scales = 1), as in the pages' timing
+    workload."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    if sm_scale is None:
+        sm_scale = 1.0 / np.sqrt(D)
+    sm_scale = float(np.float32(sm_scale))
+
+    def draw(shape):
+        if zero:
+            return np.zeros(shape, dtype=np.float32)
+        return rng.standard_normal(shape, dtype=np.float32)
+
+    qf = draw((B, S, H, D))
+    kf = draw((B, N, D))
+    wf = draw((B, S, H)) * np.float32(w_std)
+
+    q_sf = k_sf = k_tok = None
+    if fmt == FMT_BF16:
+        q, k = to_bf16_codes(qf), to_bf16_codes(kf)
+    elif fmt == FMT_E4M3:
+        # per-key scale amax/448; per-query-row scale folded into W
+        kam = np.abs(kf).max(axis=-1)
+        k_tok = np.where(kam > 0, kam / np.float32(E4M3_MAX), 1.0).astype(np.float32)
+        k = to_e4m3_codes(kf / k_tok[..., None])
+        qam = np.abs(qf).max(axis=(-1, -2))
+        q_row = np.where(qam > 0, qam / np.float32(E4M3_MAX), 1.0).astype(np.float32)
+        q = to_e4m3_codes(qf / q_row[..., None, None])
+        wf = (wf * q_row[..., None]).astype(np.float32)
+    elif fmt in (FMT_MXFP8, FMT_MXFP4):
+        elem = "e4m3" if fmt == FMT_MXFP8 else "e2m1"
+        q, q_sf = mx_quantize(qf, elem)
+        k, k_sf = mx_quantize(kf, elem)
+        if zero or mx_unit_scales:
+            q_sf = np.full_like(q_sf, 0x7F)
+            k_sf = np.full_like(k_sf, 0x7F)
+    else:
+        raise ValueError(f"unknown format {fmt}")
+
+    w = to_bf16_codes(wf) if w_fmt == W_BF16 else wf.astype(np.float32)
+
+    if ks is None or ke is None:
+        if windows == "full":
+            ks = np.zeros((B, S), dtype=np.int32)
+            ke = np.full((B, S), N, dtype=np.int32)
+        elif windows == "causal":
+            ks, ke = causal_windows(B, S, N, N - S + 1)
+        elif windows == "causal_excl":
+            ks, ke = causal_windows(B, S, N, N - S)
+        elif windows == "irregular":
+            ks, ke = irregular_windows(rng, B, S, N)
+        else:
+            raise ValueError(windows)
+    ks = np.ascontiguousarray(np.broadcast_to(np.asarray(ks, dtype=np.int32), (B, S)))
+    ke = np.ascontiguousarray(np.broadcast_to(np.asarray(ke, dtype=np.int32), (B, S)))
+    return Case(name=name or f"{FMT_NAMES[fmt]}_B{B}_S{S}_N{N}", fmt=fmt, B=B,
+                S=S, N=N, H=H, D=D, sm_scale=sm_scale, q=q, k=k, w=w,
+                w_fmt=w_fmt, ks=ks, ke=ke, q_sf=q_sf, k_sf=k_sf, k_tok=k_tok)
+
+
+# The five workloads, by what they are. Seed = position in this list.
+WORKLOADS = {
+    "tiny_causal_bf16": dict(fmt=FMT_BF16, B=1, S=128, N=1024, windows="causal",
+                             w_fmt=W_F32, seed=0),
+    "bf16_batched_causal_4096": dict(fmt=FMT_BF16, B=2, S=4096, N=4096,
+                                     windows="causal", w_fmt=W_BF16, seed=1),
+    "fp8_per_token_2048x32768": dict(fmt=FMT_E4M3, B=1, S=2048, N=32768,
+                                     windows="causal_excl", w_fmt=W_F32, seed=2),
+    "mxfp8_8192x65536": dict(fmt=FMT_MXFP8, B=1, S=8192, N=65536,
+                             windows="causal_excl", w_fmt=W_F32, seed=3),
+    "mxfp4_irregular_8192x65536": dict(fmt=FMT_MXFP4, B=1, S=8192, N=65536,
+                                       windows="irregular", w_fmt=W_F32, seed=4),
+}
+
+
+def make_workload(name: str, **overrides) -> Case:
+    kw = dict(WORKLOADS[name])
+    kw.update(overrides)
+    return make_case(name=name, **kw)
