@@ -70,6 +70,8 @@ def _load():
                                    i32, i32, i32, i32, i32, dbl, vp, i64,
                                    vp, vp, vp, i32]
         lib.orc_num_threads.restype = i32
+        lib.orc_dequant_row.restype = i32
+        lib.orc_dequant_row.argtypes = [i32, vp, vp, i32, dbl, vp]
         _lib = lib
         return lib
 
@@ -88,6 +90,16 @@ def decode_e2m1(code: int) -> float:
 
 def decode_e8m0(code: int) -> float:
     return _load().orc_decode_e8m0(code)
+
+
+def dequant_row(fmt, data, sf, D, extra=1.0):
+    """Dequantise one row of D elements (raw bytes, E8M0 scales) to float64."""
+    data = np.ascontiguousarray(data)
+    sf = None if sf is None else np.ascontiguousarray(sf, dtype=np.uint8)
+    dst = np.empty(D, dtype=np.float64)
+    if _load().orc_dequant_row(fmt, _ptr(data), _ptr(sf), D, float(extra), _ptr(dst)) != 0:
+        raise ValueError("oracle rejected its arguments")
+    return dst
 
 
 def num_threads() -> int:

@@ -255,6 +255,15 @@ int orc_logits(int fmt, int w_fmt, const void* q, const uint8_t* q_sf,
   return status;
 }
 
+/* Exported for the pins: dequantise one row (Q head or K key) of D elements. */
+int orc_dequant_row(int fmt, const uint8_t* data, const uint8_t* sf, int D,
+                    double extra, double* dst) {
+  if (!data || !dst || D < 1) return -1;
+  if ((fmt == ORC_MXFP8 || fmt == ORC_MXFP4) && (!sf || D % 32 != 0)) return -1;
+  dequant_row(fmt, data, sf, D, extra, dst);
+  return 0;
+}
+
 int orc_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

@@ -241,6 +241,22 @@ def test_fp4_nibble_order():
         assert out[0].tolist() == expect
 
 
+def test_fp4_row_dequant_nibble_order_and_blocks():
+    """Byte b of an E2M1 row holds element 2b in its low nibble and 2b+1 in
+    its high nibble (the torch float4_e2m1fn_x2 packing); element d takes the
+    E8M0 scale of block d // 32."""
+    D = 64
+    data = np.zeros(D // 2, np.uint8)
+    data[0] = 0x3A        # d0 = code 0xA (-1.0), d1 = code 0x3 (1.5)
+    data[20] = 0x71       # d40 = code 0x1 (0.5), d41 = code 0x7 (6.0)
+    sf = np.array([0x7F + 1, 0x7F - 2], np.uint8)     # x2, x0.25
+    got = oracle.dequant_row(synth.FMT_MXFP4, data, sf, D)
+    expect = np.zeros(D)
+    expect[0], expect[1] = -1.0 * 2, 1.5 * 2
+    expect[40], expect[41] = 0.5 * 0.25, 6.0 * 0.25
+    assert np.array_equal(got, expect)
+
+
 def test_mx_block_scale_locality():
     """The E8M0 byte of block b scales only dims 32b..32b+31."""
     D, N = 128, 4
