@@ -1,0 +1,162 @@
+/*
+ * dsa_indexer.h — C ABI of the GB300 (sm_103a) lightning-indexer library.
+ *
+ * The operation (one call = one pass of the indexer's MQA-logits forward):
+ *
+ *   out[b,i,j] = sum_h w[b,i,h] * ReLU(sm_scale * q[b,i,h,:] . k[b,j,:])
+ *                                              for ks[b,i] <= j < ke[b,i]
+ *   out[b,i,j] = -inf                          for every other j < N (clean != 0)
+ *
+ * H query heads share one key head of dimension D. Defined by:
+ *  - DeepGEMM pull request 435, "Improve SM100 MX MQA logits clean-output
+ *    performance": the fp8_fp4_mqa_logits call in its "Standalone performance
+ *    reproducer" section — (q, q_scales), (k, k_scales), weights, starts,
+ *    ends, clean_logits, FP32 logits; windows [0, KV-Q+row) in "Performance";
+ *    MX scales packed four E8M0 bytes per 32-bit word, 0x7f7f7f7f = all ones;
+ *    -inf outside the window and 0 in-window for all-zero inputs.
+ *  - cuDNN-frontend pull request 416, "DSA indexer forward: add a lean SM100
+ *    fast path ...", sections "What", "Precision / determinism" and "Support
+ *    surface": BF16 Q/K, BF16 or FP32 W, FP32 scores, H=64, D=128, h_kv=1,
+ *    batched uniform-length BSHD, -inf outside the window, S_q % 4 == 0,
+ *    16-byte aligned base pointers, finite sm_scale.
+ *
+ * Conventions shared by every entry point:
+ *  - Every pointer argument of a compute call is a DEVICE pointer on the
+ *    current CUDA device, owned by the caller; the library never frees it.
+ *  - Calls are asynchronous and ordered on `stream` (NULL = legacy default
+ *    stream). They never synchronise and never read device data on the host.
+ *  - A non-zero return is an idx_status; nothing was launched in that case.
+ */
+#ifndef DSA_INDEXER_H_
+#define DSA_INDEXER_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define IDX_API __attribute__((visibility("default")))
+#else
+#define IDX_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* idx_stream_t; /* same type as cudaStream_t */
+
+/* Element format of Q and K (both use the same one). */
+typedef enum idx_format {
+  IDX_FMT_BF16 = 0,  /* bfloat16 elements; D elements per row                 */
+  IDX_FMT_E4M3 = 1,  /* OCP FP8 E4M3; optional FP32 per-key scale (k_scales)   */
+  IDX_FMT_MXFP8 = 2, /* E4M3 + one E8M0 scale per 32 elements of D            */
+  IDX_FMT_MXFP4 = 3  /* E2M1, two per byte (even element in the low nibble),
+                        + one E8M0 scale per 32 elements of D                  */
+} idx_format;
+
+/* Element format of the head weights w. */
+typedef enum idx_w_format { IDX_W_F32 = 0, IDX_W_BF16 = 1 } idx_w_format;
+
+typedef enum idx_status {
+  IDX_OK = 0,
+  IDX_ERR_NULL = 1,        /* a required pointer is NULL                            */
+  IDX_ERR_SHAPE = 2,       /* H != 64, D != 128, S % 4 != 0, B/S < 1, N < 1,
+                              out_row_stride < N, or a size beyond int32 indexing    */
+  IDX_ERR_FORMAT = 3,      /* unknown fmt / w_fmt, or scales missing for MX          */
+  IDX_ERR_ALIGN = 4,       /* q/k base or row stride not 16-byte aligned              */
+  IDX_ERR_SCALE = 5,       /* sm_scale is not finite                                  */
+  IDX_ERR_DEVICE = 6,      /* current device is not compute capability 10.3 (sm_103) */
+  IDX_ERR_CUDA = 7,        /* a CUDA runtime call failed (launch, allocation, ...)   */
+  IDX_ERR_TIMEOUT = 8,     /* device-side wait gave up; the call's output is invalid */
+  IDX_ERR_UNSUPPORTED = 9  /* valid request this build does not implement            */
+} idx_status;
+
+/* Problem shape and layout. Zero strides mean "dense". */
+typedef struct idx_shape {
+  int32_t B;              /* batches (uniform length), >= 1                          */
+  int32_t S;              /* query rows per batch, multiple of 4                      */
+  int32_t N;              /* keys per batch, >= 1                                      */
+  int32_t H;              /* query heads, must be 64                                   */
+  int32_t D;              /* head dimension, must be 128                               */
+  int32_t fmt;            /* idx_format                                                */
+  int32_t w_fmt;          /* idx_w_format                                              */
+  int32_t reserved;       /* must be 0                                                 */
+  int64_t q_row_bytes;    /* bytes between consecutive (b,i,h) rows of q; 0 = dense    */
+  int64_t k_row_bytes;    /* bytes between consecutive keys of k; 0 = dense            */
+  int64_t k_batch_bytes;  /* bytes between batches of k; 0 = N * k_row_bytes           */
+  int64_t out_row_stride; /* floats between consecutive output rows; 0 = N             */
+} idx_shape;
+
+/* Compute the logits (one call of the hot path).
+ *
+ *  q        [B,S,H,D] elements (MXFP4: D/2 bytes per (b,i,h) row), row stride
+ *           q_row_bytes (multiple of 16), base 16-byte aligned; batches and
+ *           rows contiguous at that stride.
+ *  q_sf     MX formats: E8M0 bytes [B,S,H,D/32], dense (byte g of a head row
+ *           scales elements 32g..32g+31; the four bytes of a row read as a
+ *           little-endian int32 are DeepGEMM's packed q_scales); else NULL.
+ *  k        [B,N,D] elements (MXFP4: D/2 bytes per key), strides k_row_bytes
+ *           and k_batch_bytes (multiples of 16), base 16-byte aligned.
+ *  k_sf     MX formats: E8M0 bytes [B,N,D/32], dense; else NULL.
+ *  k_scales IDX_FMT_E4M3 only: FP32 [B,N] per-key scale >= 0 multiplying K
+ *           (a per-query-row Q scale belongs in w); NULL means 1. Must be NULL
+ *           for the other formats.
+ *  w        [B,S,H] FP32 or BF16 (w_fmt), dense.
+ *  ks, ke   [B,S] int32, dense. Row (b,i) sees keys [max(ks,0), min(ke,N));
+ *           ks >= ke is an empty row (all -inf). Values are clamped on the
+ *           device; any int32 is accepted.
+ *  sm_scale finite float; it multiplies the dot product inside the ReLU (a
+ *           negative value is honoured exactly: ReLU(s*x) = |s|*ReLU(-x)).
+ *  clean    non-zero: every column j < N outside the window is written -inf.
+ *           zero: columns of 128-key tiles that contain no in-window key of
+ *           any of the row's 4-row group are left untouched; the rest is
+ *           written (-inf outside the window).
+ *  out      FP32 [B,S,out_row_stride]; columns >= N are never written.
+ *  shape    see idx_shape (host pointer, read during the call only).
+ *  stream   CUDA stream of the launch.
+ *
+ * Returns IDX_OK once the work is enqueued. Argument errors are detected on
+ * the host before any launch. A device-side wait that runs out is reported
+ * by indexer_get_last_error(), not here. The first call on a (device,
+ * stream) pair allocates a small library-owned scratch block (a few hundred
+ * bytes: a work counter and an error word), so make one call before
+ * capturing a CUDA graph on that stream; calls on one stream reuse it, so
+ * calls on the same stream must not overlap (stream order guarantees that).
+ */
+IDX_API int indexer_logits(const void* q, const uint8_t* q_sf, const void* k, const uint8_t* k_sf,
+                   const float* k_scales, const void* w, const int32_t* ks, const int32_t* ke,
+                   float sm_scale, int clean, float* out, const idx_shape* shape,
+                   idx_stream_t stream);
+
+/* Human-readable text for an idx_status value (static storage, never NULL). */
+IDX_API const char* indexer_status_string(int status);
+
+/* Synchronise `stream`, then return and clear the device-side error word of
+ * that (current device, stream) pair: IDX_OK, or IDX_ERR_TIMEOUT if a kernel
+ * on it gave up waiting (its output is then invalid). Returns IDX_OK when no
+ * call was ever made on the pair, IDX_ERR_CUDA if synchronisation fails. */
+IDX_API int indexer_get_last_error(idx_stream_t stream);
+
+/* Device-side wait limit in nanoseconds for later launches from this process
+ * (default 2e9). Used by tests to make a wait run out on purpose; values
+ * below 1e6 are raised to 1e6. Returns the previous value. */
+IDX_API int64_t indexer_set_wait_limit_ns(int64_t ns);
+
+/* Number of kernel launches one indexer_logits call makes (for launch counts
+ * in benchmarks). */
+IDX_API int indexer_launches_per_call(void);
+
+/* Free every library-owned scratch block on every device (synchronises each
+ * device that has one). Later calls allocate again. Returns IDX_OK or
+ * IDX_ERR_CUDA. */
+IDX_API int indexer_shutdown(void);
+
+/* Library ABI version: major*10000 + minor*100 + patch. */
+IDX_API int indexer_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_INDEXER_H_ */

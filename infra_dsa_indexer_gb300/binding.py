@@ -1,0 +1,163 @@
+"""Thin ctypes binding over the C ABI in include/dsa_indexer.h.
+
+Same entry-point names as the C library; this module only marshals torch
+tensors into pointers and shape structs and raises on a non-zero status. All
+arithmetic runs in the CUDA library. If the library has not been built
+(infra_dsa_indexer_gb300/_build/libdsa_indexer.so), every call raises; there
+is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+import torch
+
+IDX_FMT_BF16, IDX_FMT_E4M3, IDX_FMT_MXFP8, IDX_FMT_MXFP4 = 0, 1, 2, 3
+IDX_W_F32, IDX_W_BF16 = 0, 1
+IDX_OK = 0
+IDX_ERR_TIMEOUT = 8
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build",
+                         "libdsa_indexer.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class IndexerError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: status {status} ({indexer_status_string(status)})")
+
+
+class idx_shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("S", ctypes.c_int32), ("N", ctypes.c_int32),
+                ("H", ctypes.c_int32), ("D", ctypes.c_int32), ("fmt", ctypes.c_int32),
+                ("w_fmt", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("q_row_bytes", ctypes.c_int64), ("k_row_bytes", ctypes.c_int64),
+                ("k_batch_bytes", ctypes.c_int64), ("out_row_stride", ctypes.c_int64)]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Open the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"CUDA library not built: {_LIB_PATH} is missing "
+                "(run `python -m infra_dsa_indexer_gb300.build`)")
+        lib = ctypes.CDLL(_LIB_PATH)
+        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        lib.indexer_logits.restype = i32
+        lib.indexer_logits.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, i32,
+                                       vp, ctypes.POINTER(idx_shape), vp]
+        lib.indexer_status_string.restype = ctypes.c_char_p
+        lib.indexer_status_string.argtypes = [i32]
+        lib.indexer_get_last_error.restype = i32
+        lib.indexer_get_last_error.argtypes = [vp]
+        lib.indexer_set_wait_limit_ns.restype = i64
+        lib.indexer_set_wait_limit_ns.argtypes = [i64]
+        lib.indexer_launches_per_call.restype = i32
+        lib.indexer_launches_per_call.argtypes = []
+        lib.indexer_shutdown.restype = i32
+        lib.indexer_shutdown.argtypes = []
+        lib.indexer_version.restype = i32
+        lib.indexer_version.argtypes = []
+        _lib = lib
+        return lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("indexer_logits takes CUDA tensors (device pointers)")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def make_shape(B, S, N, H, D, fmt, w_fmt, *, q_row_bytes=0, k_row_bytes=0,
+               k_batch_bytes=0, out_row_stride=0) -> idx_shape:
+    return idx_shape(B, S, N, H, D, fmt, w_fmt, 0, q_row_bytes, k_row_bytes,
+                     k_batch_bytes, out_row_stride)
+
+
+def indexer_logits(q, q_sf, k, k_sf, k_scales, w, ks, ke, sm_scale, clean, out,
+                   shape: idx_shape, stream=None) -> None:
+    """Enqueue one logits call. Tensors are CUDA tensors holding the raw
+    layouts of include/dsa_indexer.h (q [B,S,H,row], k [B,N,row], w [B,S,H],
+    ks/ke [B,S] int32, out [B,S,>=N] float32); q_sf/k_sf/k_scales may be None."""
+    lib = load()
+    st = lib.indexer_logits(_ptr(q), _ptr(q_sf), _ptr(k), _ptr(k_sf), _ptr(k_scales), _ptr(w),
+                            _ptr(ks), _ptr(ke), ctypes.c_float(sm_scale), int(bool(clean)),
+                            _ptr(out), ctypes.byref(shape), _stream(stream))
+    if st != IDX_OK:
+        raise IndexerError(st, "indexer_logits")
+
+
+def indexer_status_string(status: int) -> str:
+    return load().indexer_status_string(int(status)).decode()
+
+
+def indexer_get_last_error(stream=None) -> int:
+    return load().indexer_get_last_error(_stream(stream))
+
+
+def indexer_set_wait_limit_ns(ns: int) -> int:
+    return load().indexer_set_wait_limit_ns(int(ns))
+
+
+def indexer_launches_per_call() -> int:
+    return load().indexer_launches_per_call()
+
+
+def indexer_shutdown() -> int:
+    return load().indexer_shutdown()
+
+
+def indexer_version() -> int:
+    return load().indexer_version()
+
+
+# ---------------------------------------------------------------------------
+# convenience: a synth.Case on the device
+# ---------------------------------------------------------------------------
+
+def case_to_device(case, device="cuda", out_row_stride=None):
+    """Copy a synth.Case's input bytes to `device`; allocate the FP32 output."""
+    def dev(a):
+        if a is None:
+            return None
+        if a.dtype == np.uint16:          # bf16 codes travel as int16 bit patterns
+            a = a.view(np.int16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    t = dict(q=dev(case.q), k=dev(case.k), w=dev(case.w), ks=dev(case.ks), ke=dev(case.ke),
+             q_sf=dev(case.q_sf), k_sf=dev(case.k_sf), k_scales=dev(case.k_tok))
+    stride = out_row_stride or case.N
+    t["out"] = torch.empty((case.B, case.S, stride), dtype=torch.float32, device=device)
+    t["shape"] = make_shape(case.B, case.S, case.N, case.H, case.D, case.fmt, case.w_fmt,
+                            out_row_stride=stride)
+    return t
+
+
+def run_case(case, t, stream=None, clean=None):
+    """indexer_logits on tensors made by case_to_device."""
+    indexer_logits(t["q"], t["q_sf"], t["k"], t["k_sf"], t["k_scales"], t["w"], t["ks"],
+                   t["ke"], case.sm_scale, case.clean if clean is None else clean, t["out"],
+                   t["shape"], stream)
+    return t["out"]

@@ -1,0 +1,280 @@
+// Host side of the C ABI declared in include/dsa_indexer.h: argument checks,
+// TMA tensor maps, per-(device, stream) scratch, the persistent launch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <algorithm>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "dsa_indexer.h"
+#include "indexer_kernel.cuh"
+
+namespace {
+
+using dsa::KernelParams;
+
+constexpr int kScratchInts = 64;  // 256 bytes per (device, stream)
+
+struct DeviceInfo {
+  bool valid = false;
+  int sm_count = 0;
+  int cc_major = 0, cc_minor = 0;
+  bool smem_set[4] = {false, false, false, false};
+};
+
+std::mutex g_mutex;
+std::map<int, DeviceInfo> g_devices;
+std::map<std::pair<int, uintptr_t>, int32_t*> g_scratch;
+int64_t g_wait_limit_ns = 2000000000LL;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int get_device_info(int dev, DeviceInfo** out) {
+  DeviceInfo& di = g_devices[dev];
+  if (!di.valid) {
+    if (cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&di.cc_major, cudaDevAttrComputeCapabilityMajor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&di.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) !=
+            cudaSuccess)
+      return IDX_ERR_CUDA;
+    di.valid = true;
+  }
+  *out = &di;
+  return IDX_OK;
+}
+
+int get_encoder() {
+  if (g_encode) return IDX_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return IDX_ERR_CUDA;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return IDX_OK;
+}
+
+int get_scratch(int dev, cudaStream_t stream, int32_t** out) {
+  auto key = std::make_pair(dev, reinterpret_cast<uintptr_t>(stream));
+  auto it = g_scratch.find(key);
+  if (it != g_scratch.end()) {
+    *out = it->second;
+    return IDX_OK;
+  }
+  int32_t* p = nullptr;
+  if (cudaMalloc(&p, kScratchInts * sizeof(int32_t)) != cudaSuccess) return IDX_ERR_CUDA;
+  if (cudaMemset(p, 0, kScratchInts * sizeof(int32_t)) != cudaSuccess) {
+    cudaFree(p);
+    return IDX_ERR_CUDA;
+  }
+  g_scratch[key] = p;
+  *out = p;
+  return IDX_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 2-D or 3-D tiled map with 128-byte swizzle. dims/strides in elements/bytes.
+int encode_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int rank,
+               const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box) {
+  uint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, dtype, rank, const_cast<void*>(base), dims, strides_bytes, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? IDX_OK : IDX_ERR_CUDA;
+}
+
+template <int FMT>
+int launch(const KernelParams& prm, int grid, DeviceInfo* di, cudaStream_t stream) {
+  constexpr int smem = dsa::Layout<FMT>::kBytes;
+  auto kern = dsa::indexer_logits_kernel<FMT>;
+  if (!di->smem_set[FMT]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return IDX_ERR_CUDA;
+    di->smem_set[FMT] = true;
+  }
+  kern<<<grid, dsa::kThreads, smem, stream>>>(prm);
+  return cudaGetLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int indexer_version(void) { return 100; }
+
+int indexer_launches_per_call(void) { return 1; }
+
+const char* indexer_status_string(int status) {
+  switch (status) {
+    case IDX_OK: return "ok";
+    case IDX_ERR_NULL: return "a required pointer is NULL";
+    case IDX_ERR_SHAPE: return "unsupported or inconsistent shape (H must be 64, D 128, S % 4 == 0, N >= 1, out_row_stride >= N)";
+    case IDX_ERR_FORMAT: return "unknown format, or scales missing/present for the wrong format";
+    case IDX_ERR_ALIGN: return "q/k base address or row stride is not 16-byte aligned";
+    case IDX_ERR_SCALE: return "sm_scale is not finite";
+    case IDX_ERR_DEVICE: return "current device is not compute capability 10.3 (sm_103)";
+    case IDX_ERR_CUDA: return "a CUDA runtime call failed";
+    case IDX_ERR_TIMEOUT: return "a device-side wait ran out; the output of that call is invalid";
+    case IDX_ERR_UNSUPPORTED: return "request not supported by this build";
+    default: return "unknown status";
+  }
+}
+
+int64_t indexer_set_wait_limit_ns(int64_t ns) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  const int64_t prev = g_wait_limit_ns;
+  g_wait_limit_ns = ns < 1000000 ? 1000000 : ns;
+  return prev;
+}
+
+int indexer_logits(const void* q, const uint8_t* q_sf, const void* k, const uint8_t* k_sf,
+                   const float* k_scales, const void* w, const int32_t* ks, const int32_t* ke,
+                   float sm_scale, int clean, float* out, const idx_shape* shape,
+                   idx_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (!shape || !q || !k || !w || !ks || !ke || !out) return IDX_ERR_NULL;
+  const idx_shape sh = *shape;
+  if (sh.fmt < IDX_FMT_BF16 || sh.fmt > IDX_FMT_MXFP4) return IDX_ERR_FORMAT;
+  if (sh.w_fmt != IDX_W_F32 && sh.w_fmt != IDX_W_BF16) return IDX_ERR_FORMAT;
+  const bool mx = sh.fmt == IDX_FMT_MXFP8 || sh.fmt == IDX_FMT_MXFP4;
+  if (mx && (!q_sf || !k_sf)) return IDX_ERR_NULL;
+  if (!mx && (q_sf || k_sf)) return IDX_ERR_FORMAT;
+  if (k_scales && sh.fmt != IDX_FMT_E4M3) return IDX_ERR_FORMAT;
+  if (sh.H != dsa::kHeads || sh.D != dsa::kHeadDim || sh.reserved != 0) return IDX_ERR_SHAPE;
+  if (sh.B < 1 || sh.S < 1 || sh.S % dsa::kRowsPerBlock != 0 || sh.N < 1) return IDX_ERR_SHAPE;
+  if (!std::isfinite(sm_scale)) return IDX_ERR_SCALE;
+
+  const int64_t elem_row_bytes =
+      sh.fmt == IDX_FMT_BF16 ? 2 * sh.D : (sh.fmt == IDX_FMT_MXFP4 ? sh.D / 2 : sh.D);
+  const int64_t q_row = sh.q_row_bytes ? sh.q_row_bytes : elem_row_bytes;
+  const int64_t k_row = sh.k_row_bytes ? sh.k_row_bytes : elem_row_bytes;
+  const int64_t k_batch = sh.k_batch_bytes ? sh.k_batch_bytes : k_row * sh.N;
+  const int64_t out_stride = sh.out_row_stride ? sh.out_row_stride : sh.N;
+  if (q_row < elem_row_bytes || k_row < elem_row_bytes || k_batch < k_row * sh.N ||
+      out_stride < sh.N)
+    return IDX_ERR_SHAPE;
+  const int64_t total_rows = static_cast<int64_t>(sh.B) * sh.S;
+  if (total_rows * sh.H >= (int64_t(1) << 31) || static_cast<int64_t>(sh.B) * sh.N >= (int64_t(1) << 31))
+    return IDX_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(k) || q_row % 16 || k_row % 16 || k_batch % 16)
+    return IDX_ERR_ALIGN;
+  if (sh.fmt == IDX_FMT_MXFP8 || sh.fmt == IDX_FMT_MXFP4) return IDX_ERR_UNSUPPORTED;
+
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return IDX_ERR_CUDA;
+  DeviceInfo* di = nullptr;
+  int st = get_device_info(dev, &di);
+  if (st) return st;
+  if (di->cc_major != 10 || di->cc_minor != 3) return IDX_ERR_DEVICE;
+  if ((st = get_encoder())) return st;
+  int32_t* scratch = nullptr;
+  if ((st = get_scratch(dev, stream, &scratch))) return st;
+
+  KernelParams prm;
+  std::memset(&prm, 0, sizeof(prm));
+  const CUtensorMapDataType dt =
+      sh.fmt == IDX_FMT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const uint32_t panel_elems = sh.fmt == IDX_FMT_BF16 ? 64 : 128;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(sh.D), static_cast<uint64_t>(total_rows * sh.H)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(q_row)};
+    const uint32_t box[2] = {panel_elems, static_cast<uint32_t>(dsa::kBlockN)};
+    if ((st = encode_map(&prm.tmap_q, q, dt, 2, dims, strides, box))) return st;
+  }
+  {
+    const uint64_t dims[3] = {static_cast<uint64_t>(sh.D), static_cast<uint64_t>(sh.N),
+                              static_cast<uint64_t>(sh.B)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(k_row), static_cast<uint64_t>(k_batch)};
+    const uint32_t box[3] = {panel_elems, static_cast<uint32_t>(dsa::kKeysPerTile), 1};
+    if ((st = encode_map(&prm.tmap_k, k, dt, 3, dims, strides, box))) return st;
+  }
+  prm.q_sf = q_sf;
+  prm.k_sf = k_sf;
+  prm.k_scales = k_scales;
+  prm.w = w;
+  prm.ks = ks;
+  prm.ke = ke;
+  prm.out = out;
+  prm.scratch = scratch;
+  prm.out_row_stride = out_stride;
+  prm.B = sh.B;
+  prm.S = sh.S;
+  prm.N = sh.N;
+  prm.w_bf16 = sh.w_fmt == IDX_W_BF16;
+  prm.clean = clean != 0;
+  prm.sm_scale = sm_scale;
+  prm.blocks_per_batch = sh.S / dsa::kRowsPerBlock;
+  prm.timeout_ns = static_cast<uint64_t>(g_wait_limit_ns);
+
+  // Units: every row-block split into nchunk pieces of its key tiles. Long
+  // rows get pieces of at most ~64 tiles (load balance across the persistent
+  // grid); small problems get enough pieces for about two per SM.
+  const int64_t row_blocks = total_rows / dsa::kRowsPerBlock;
+  const int64_t tiles_max = (sh.N + dsa::kKeysPerTile - 1) / dsa::kKeysPerTile;
+  int64_t nchunk = (tiles_max + 63) / 64;
+  const int64_t want = (2 * di->sm_count + row_blocks - 1) / row_blocks;
+  nchunk = std::max<int64_t>(nchunk, std::min<int64_t>(want, tiles_max));
+  nchunk = std::max<int64_t>(nchunk, 1);
+  const int64_t units = row_blocks * nchunk;
+  if (units >= (int64_t(1) << 30)) return IDX_ERR_SHAPE;
+  prm.nchunk = static_cast<int32_t>(nchunk);
+  prm.num_units = static_cast<int32_t>(units);
+  const int grid = static_cast<int>(std::min<int64_t>(di->sm_count, units));
+
+  switch (sh.fmt) {
+    case IDX_FMT_BF16: return launch<dsa::kFmtBF16>(prm, grid, di, stream);
+    case IDX_FMT_E4M3: return launch<dsa::kFmtE4M3>(prm, grid, di, stream);
+    default: return IDX_ERR_UNSUPPORTED;
+  }
+}
+
+int indexer_get_last_error(idx_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return IDX_ERR_CUDA;
+  int32_t* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    auto it = g_scratch.find(std::make_pair(dev, reinterpret_cast<uintptr_t>(stream)));
+    if (it == g_scratch.end()) return IDX_OK;
+    scratch = it->second;
+  }
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return IDX_ERR_CUDA;
+  int32_t word = 0;
+  if (cudaMemcpy(&word, scratch + 2, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return IDX_ERR_CUDA;
+  if (word != 0) {
+    const int32_t zero[3] = {0, 0, 0};
+    // A run that gave up may leave the unit counter and the CTA count behind.
+    if (cudaMemcpy(scratch, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return IDX_ERR_CUDA;
+  }
+  return word == 0 ? IDX_OK : (word == dsa::kErrTimeout ? IDX_ERR_TIMEOUT : word);
+}
+
+int indexer_shutdown(void) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int rc = IDX_OK;
+  int cur = 0;
+  cudaGetDevice(&cur);
+  for (auto& kv : g_scratch) {
+    if (cudaSetDevice(kv.first.first) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess ||
+        cudaFree(kv.second) != cudaSuccess)
+      rc = IDX_ERR_CUDA;
+  }
+  g_scratch.clear();
+  cudaSetDevice(cur);
+  return rc;
+}
+
+}  // extern "C"

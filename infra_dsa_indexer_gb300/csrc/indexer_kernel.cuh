@@ -1,0 +1,467 @@
+// Lightning-indexer MQA-logits forward, one persistent warp-specialised
+// kernel for sm_103a.
+//
+//   out[b,i,j] = sum_h w[b,i,h] * ReLU(sm_scale * q[b,i,h,:] . k[b,j,:])  (ks <= j < ke)
+//   out[b,i,j] = -inf                                                     (otherwise)
+//
+// The operation is the "fp8_fp4_mqa_logits" call of DeepGEMM pull request 435
+// ("Improve SM100 MX MQA logits clean-output performance", standalone
+// performance reproducer) and the BF16 indexer forward of cuDNN-frontend pull
+// request 416 ("DSA indexer forward: add a lean SM100 fast path ...",
+// sections "What" and "Precision / determinism").
+//
+// Work decomposition (own design; the pages' kernels are prior art):
+//  * row-block = 4 consecutive query rows of one batch = 4 x 64 heads = 256
+//    (row, head) pairs; key tile = 128 keys.
+//  * One tcgen05 MMA group per (row-block, key tile) with swapped operands:
+//    A = key tile (M = 128 keys), B = the row-block's Q (N = 256 (row,head)),
+//    K = D = 128. The FP32 accumulator lands in TMEM with one key per lane and
+//    one (row, head) per column, so the head reduction sum_h w*ReLU(s*x) is a
+//    per-thread loop over columns: no shuffles, no shared-memory reduction.
+//  * A unit of work is (row-block, chunk of its key tiles). Units are handed
+//    out through a global atomic counter, longest row-blocks first (for causal
+//    windows the highest row index), so the persistent grid balances itself.
+//
+// Roles (384 threads, one CTA per SM):
+//  warp 0       scheduler + TMA producer (one elected lane)
+//  warp 1       TMEM allocator + MMA issuer (one elected lane)
+//  warps 2-3    idle
+//  warps 4-11   epilogue: TMEM -> registers, ReLU.w head sum, masked FP32
+//               stores, -inf fill of columns outside the row-block's tiles.
+//               Warp w reads TMEM lanes 32*(w%4)..+31 (the sub-partition it
+//               may access); warps 4-7 own rows 0,1 of the block, 8-11 rows 2,3.
+// Pipelines (mbarriers): unit slots x2 (unit info + Q block), key-tile ring
+// (STAGES), TMEM accumulators x2 (2 x 256 columns), so the MMA of tile t+1
+// overlaps the epilogue of tile t.
+#pragma once
+#include <cuda.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace dsa {
+
+constexpr int kKeysPerTile = 128;  // MMA M
+constexpr int kRowsPerBlock = 4;
+constexpr int kHeads = 64;
+constexpr int kBlockN = kRowsPerBlock * kHeads;  // MMA N = 256
+constexpr int kHeadDim = 128;                    // MMA K per tile
+constexpr int kThreads = 384;
+constexpr int kEpiWarp0 = 4;
+constexpr int kNumEpiWarps = 8;
+constexpr int kNumEpiThreads = kNumEpiWarps * 32;
+constexpr uint32_t kTmemCols = 512;
+
+enum : int { kFmtBF16 = 0, kFmtE4M3 = 1, kFmtMXFP8 = 2, kFmtMXFP4 = 3 };
+enum : int { kErrTimeout = 8, kErrAlign = 4 };
+
+struct UnitInfo {
+  int32_t stop;
+  int32_t b;
+  int32_t grow0;     // flattened row id b*S + i of the block's first row
+  int32_t c0, c1;    // key tiles [c0, c1) computed by this unit
+  int32_t t0, t1;    // key tiles [t0, t1) covered by the whole row-block
+  int32_t flags;     // bit 0: fill [0, t0*128) with -inf; bit 1: fill [t1*128, N)
+  int32_t lo[4];     // clamped window per row
+  int32_t hi[4];
+};
+
+struct KernelParams {
+  CUtensorMap tmap_q;  // [B*S*H rows, D] view of Q
+  CUtensorMap tmap_k;  // [B, N, D] view of K
+  const uint8_t* q_sf;
+  const uint8_t* k_sf;
+  const float* k_scales;
+  const void* w;
+  const int32_t* ks;
+  const int32_t* ke;
+  float* out;
+  int32_t* scratch;  // [0] unit counter, [1] finished CTAs, [2] error word
+  int64_t out_row_stride;
+  int32_t B, S, N;
+  int32_t w_bf16;
+  int32_t clean;
+  int32_t num_units;
+  int32_t nchunk;
+  int32_t blocks_per_batch;  // S / 4
+  float sm_scale;
+  uint64_t timeout_ns;
+};
+
+template <int FMT>
+struct Traits;
+
+template <>
+struct Traits<kFmtBF16> {
+  static constexpr int kRowBytes = kHeadDim * 2;        // 256 B per key / head row
+  static constexpr int kPanelElems = 64;                // 128-byte swizzle span
+  static constexpr int kPanels = 2;
+  static constexpr int kMmaK = 16;
+  static constexpr int kStages = 3;
+  static constexpr uint32_t kIdesc = instr_desc(1, 1, kKeysPerTile, kBlockN);  // BF16 x BF16
+  static constexpr int kKind = 0;
+};
+
+template <>
+struct Traits<kFmtE4M3> {
+  static constexpr int kRowBytes = kHeadDim;
+  static constexpr int kPanelElems = 128;
+  static constexpr int kPanels = 1;
+  static constexpr int kMmaK = 32;
+  static constexpr int kStages = 6;
+  static constexpr uint32_t kIdesc = instr_desc(0, 0, kKeysPerTile, kBlockN);  // E4M3 x E4M3
+  static constexpr int kKind = 1;
+};
+
+template <int FMT>
+struct Layout {
+  using T = Traits<FMT>;
+  static constexpr int kPanelRowBytes = T::kRowBytes / T::kPanels;               // 128
+  static constexpr int kKPanelBytes = kKeysPerTile * kPanelRowBytes;
+  static constexpr int kQPanelBytes = kBlockN * kPanelRowBytes;
+  static constexpr int kKTileBytes = kKPanelBytes * T::kPanels;
+  static constexpr int kQBlockBytes = kQPanelBytes * T::kPanels;
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + 2 * kQBlockBytes;
+  static constexpr int kWOff = kKOff + T::kStages * kKTileBytes;
+  static constexpr int kInfoOff = kWOff + 2 * kRowsPerBlock * kHeads * 4;
+  static constexpr int kBarOff = kInfoOff + 2 * (int)sizeof(UnitInfo);
+  static constexpr int kNumBars = 2 + 2 + 2 * T::kStages + 2 + 2 + 2;
+  static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
+  static constexpr int kBytes = kMiscOff + 16;
+};
+
+__device__ __forceinline__ int clampi(int v, int lo, int hi) {
+  return v < lo ? lo : (v > hi ? hi : v);
+}
+
+__device__ __forceinline__ void raise_error(int32_t* scratch, volatile int* abort_flag, int code) {
+  *abort_flag = 1;
+  atomicExch(scratch + 2, code);
+}
+
+// Write -inf to columns [a, b) of one output row; the 128 threads of the
+// four warps sharing `row` cover 128 consecutive columns per step.
+__device__ __forceinline__ void fill_neg_inf(float* row, int a, int b, int tid128) {
+  const float ninf = __int_as_float(0xff800000);
+  for (int j = a + tid128; j < b; j += 128) __stcs(row + j, ninf);
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 1)
+    indexer_logits_kernel(const __grid_constant__ KernelParams p) {
+  using T = Traits<FMT>;
+  using L = Layout<FMT>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+
+  uint8_t* qbuf = smem + L::kQOff;
+  uint8_t* kbuf = smem + L::kKOff;
+  float* w_s = reinterpret_cast<float*>(smem + L::kWOff);
+  UnitInfo* info = reinterpret_cast<UnitInfo*>(smem + L::kInfoOff);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* unit_full = bars;
+  uint64_t* unit_empty = bars + 2;
+  uint64_t* k_full = bars + 4;
+  uint64_t* k_empty = k_full + T::kStages;
+  uint64_t* acc_full = k_empty + T::kStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* w_ready = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    if ((smem_u32(smem) & 1023u) != 0) {
+      // The 128-byte swizzle atoms need a 1024-byte aligned base.
+      atomicExch(p.scratch + 2, kErrAlign);
+    }
+    *abort_flag = 0;
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&unit_full[s], 1);
+      mbar_init(&unit_empty[s], 1 + kNumEpiWarps);
+      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_empty[s], kNumEpiWarps);
+      mbar_init(&w_ready[s], kNumEpiThreads);
+    }
+    for (int s = 0; s < T::kStages; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const bool misaligned = (smem_u32(smem) & 1023u) != 0;
+
+  if (!misaligned && warp == 0 && lane == 0) {
+    // ---------------------------------------------------------------- producer
+    prefetch_tmap(&p.tmap_q);
+    prefetch_tmap(&p.tmap_k);
+    const uint64_t pol_k = policy_evict_last();   // K is re-read by every row-block
+    const uint64_t pol_q = policy_evict_first();  // Q block is read once per unit
+    uint32_t kiter = 0;
+    for (uint32_t it = 0;; ++it) {
+      const int slot = it & 1;
+      if (!mbar_wait(&unit_empty[slot], ((it >> 1) & 1) ^ 1, abort_flag, p.timeout_ns)) {
+        raise_error(p.scratch, abort_flag, kErrTimeout);
+        break;
+      }
+      const int u = atomicAdd(p.scratch + 0, 1);
+      UnitInfo& in = info[slot];
+      if (u >= p.num_units) {
+        in.stop = 1;
+        mbar_arrive(&unit_full[slot]);
+        break;
+      }
+      // Units in order: row-blocks from the last (longest causal window) to
+      // the first, batches interleaved, chunks of one row-block adjacent.
+      const int order = u / p.nchunk;
+      const int chunk = u - order * p.nchunk;
+      const int blk = p.blocks_per_batch - 1 - order / p.B;
+      const int b = order % p.B;
+      const int grow0 = b * p.S + blk * kRowsPerBlock;
+      int lo_all = p.N, hi_all = 0;
+      for (int r = 0; r < kRowsPerBlock; ++r) {
+        const int lo = clampi(__ldg(p.ks + grow0 + r), 0, p.N);
+        const int hi = clampi(__ldg(p.ke + grow0 + r), 0, p.N);
+        in.lo[r] = lo;
+        in.hi[r] = hi;
+        if (lo < hi) {
+          lo_all = min(lo_all, lo);
+          hi_all = max(hi_all, hi);
+        }
+      }
+      int t0 = 0, t1 = 0;
+      if (lo_all < hi_all) {
+        t0 = lo_all / kKeysPerTile;
+        t1 = (hi_all + kKeysPerTile - 1) / kKeysPerTile;
+      }
+      const int len = (t1 - t0 + p.nchunk - 1) / p.nchunk;
+      int c0 = min(t1, t0 + chunk * len);
+      int c1 = min(t1, c0 + len);
+      in.stop = 0;
+      in.b = b;
+      in.grow0 = grow0;
+      in.c0 = c0;
+      in.c1 = c1;
+      in.t0 = t0;
+      in.t1 = t1;
+      in.flags = (chunk == 0 ? 1 : 0) | (chunk == p.nchunk - 1 ? 2 : 0);
+      if (c1 > c0) {
+        mbar_arrive_expect_tx(&unit_full[slot], L::kQBlockBytes);
+        uint8_t* qdst = qbuf + slot * L::kQBlockBytes;
+        for (int pnl = 0; pnl < T::kPanels; ++pnl)
+          tma_load_2d(qdst + pnl * L::kQPanelBytes, &p.tmap_q, &unit_full[slot],
+                      pnl * T::kPanelElems, grow0 * kHeads, pol_q);
+      } else {
+        mbar_arrive(&unit_full[slot]);
+      }
+      bool ok = true;
+      for (int t = c0; t < c1; ++t, ++kiter) {
+        const int st = kiter % T::kStages;
+        if (!mbar_wait(&k_empty[st], ((kiter / T::kStages) & 1) ^ 1, abort_flag,
+                       p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&k_full[st], L::kKTileBytes);
+        uint8_t* kdst = kbuf + st * L::kKTileBytes;
+        for (int pnl = 0; pnl < T::kPanels; ++pnl)
+          tma_load_3d(kdst + pnl * L::kKPanelBytes, &p.tmap_k, &k_full[st],
+                      pnl * T::kPanelElems, t * kKeysPerTile, b, pol_k);
+      }
+      if (!ok) {
+        raise_error(p.scratch, abort_flag, kErrTimeout);
+        break;
+      }
+    }
+  } else if (!misaligned && warp == 1 && lane == 0) {
+    // --------------------------------------------------------------- MMA issuer
+    uint32_t kiter = 0, aiter = 0;
+    for (uint32_t it = 0;; ++it) {
+      const int slot = it & 1;
+      if (!mbar_wait(&unit_full[slot], (it >> 1) & 1, abort_flag, p.timeout_ns)) {
+        raise_error(p.scratch, abort_flag, kErrTimeout);
+        break;
+      }
+      const UnitInfo& in = info[slot];
+      if (in.stop) break;
+      const int c0 = in.c0, c1 = in.c1;
+      const uint32_t q_addr = smem_u32(qbuf + slot * L::kQBlockBytes);
+      bool ok = true;
+      for (int t = c0; t < c1; ++t, ++kiter, ++aiter) {
+        const int st = kiter % T::kStages;
+        const int acc = aiter & 1;
+        if (!mbar_wait(&k_full[st], (kiter / T::kStages) & 1, abort_flag, p.timeout_ns) ||
+            !mbar_wait(&acc_empty[acc], ((aiter >> 1) & 1) ^ 1, abort_flag, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(kbuf + st * L::kKTileBytes);
+        const uint32_t d_tmem = tmem_base + acc * kBlockN;
+        constexpr int kStepsPerPanel = T::kPanelElems / T::kMmaK;
+        constexpr int kStepBytes = T::kMmaK * (T::kRowBytes / kHeadDim);  // 32 B
+#pragma unroll
+        for (int kk = 0; kk < T::kPanels * kStepsPerPanel; ++kk) {
+          const int pnl = kk / kStepsPerPanel;
+          const uint32_t off = (kk % kStepsPerPanel) * kStepBytes;
+          const uint64_t a_desc = smem_desc(k_addr + pnl * L::kKPanelBytes + off, 1024, 2);
+          const uint64_t b_desc = smem_desc(q_addr + pnl * L::kQPanelBytes + off, 1024, 2);
+          tc_mma<T::kKind>(d_tmem, a_desc, b_desc, T::kIdesc, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&k_empty[st]);
+        tc_commit(&acc_full[acc]);
+      }
+      if (!ok) {
+        raise_error(p.scratch, abort_flag, kErrTimeout);
+        break;
+      }
+      tc_commit(&unit_empty[slot]);
+    }
+  } else if (!misaligned && warp >= kEpiWarp0) {
+    // ---------------------------------------------------------------- epilogue
+    const int ew = warp - kEpiWarp0;         // 0..7
+    const int et = threadIdx.x - kEpiWarp0 * 32;  // 0..255
+    const int quarter = warp & 3;            // TMEM sub-partition of this warp
+    const int pair = ew >> 2;                // rows 2*pair, 2*pair+1
+    const int tid128 = quarter * 32 + lane;  // index among the 4 warps of a pair
+    const bool neg = p.sm_scale < 0.f;
+    const float ninf = __int_as_float(0xff800000);
+    uint32_t aiter = 0;
+    for (uint32_t it = 0;; ++it) {
+      const int slot = it & 1;
+      if (!mbar_wait(&unit_full[slot], (it >> 1) & 1, abort_flag, p.timeout_ns)) {
+        raise_error(p.scratch, abort_flag, kErrTimeout);
+        break;
+      }
+      const UnitInfo in = info[slot];
+      if (in.stop) break;
+      // Stage this unit's head weights (4 rows x 64 heads) as FP32.
+      float* ws = w_s + slot * kRowsPerBlock * kHeads;
+      {
+        const int64_t widx = static_cast<int64_t>(in.grow0) * kHeads + et;
+        float wv;
+        if (p.w_bf16) {
+          const uint16_t bits = __ldg(reinterpret_cast<const uint16_t*>(p.w) + widx);
+          wv = __uint_as_float(static_cast<uint32_t>(bits) << 16);
+        } else {
+          wv = __ldg(reinterpret_cast<const float*>(p.w) + widx);
+        }
+        ws[et] = wv;
+      }
+      // All epilogue threads see all 256 weights (bounded wait, no named barrier).
+      mbar_arrive(&w_ready[slot]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&unit_empty[slot]);
+      if (!mbar_wait(&w_ready[slot], (it >> 1) & 1, abort_flag, p.timeout_ns)) {
+        raise_error(p.scratch, abort_flag, kErrTimeout);
+        break;
+      }
+
+      const int r0 = 2 * pair;
+      float* orow[2];
+      int lo[2], hi[2];
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        orow[rr] = p.out + static_cast<int64_t>(in.grow0 + r0 + rr) * p.out_row_stride;
+        lo[rr] = in.lo[r0 + rr];
+        hi[rr] = in.hi[r0 + rr];
+      }
+      if (p.clean && (in.flags & 1)) {
+        for (int rr = 0; rr < 2; ++rr) fill_neg_inf(orow[rr], 0, in.t0 * kKeysPerTile, tid128);
+      }
+      bool ok = true;
+      for (int t = in.c0; t < in.c1; ++t, ++aiter) {
+        const int acc = aiter & 1;
+        if (!mbar_wait(&acc_full[acc], (aiter >> 1) & 1, abort_flag, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int j = t * kKeysPerTile + quarter * 32 + lane;
+        float scale = p.sm_scale;
+        if (FMT == kFmtE4M3 && p.k_scales != nullptr && j < p.N)
+          scale *= __ldg(p.k_scales + static_cast<int64_t>(in.b) * p.N + j);
+        float val[2];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          uint32_t v[64];
+          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                 acc * kBlockN + (r0 + rr) * kHeads;
+          __syncwarp();  // tcgen05.ld is warp-collective: converge first
+          tmem_ld_64cols(taddr, v);
+          if (rr == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+          }
+          const float4* w4 = reinterpret_cast<const float4*>(ws + (r0 + rr) * kHeads);
+          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+          if (!neg) {
+#pragma unroll
+            for (int h4 = 0; h4 < kHeads / 4; ++h4) {
+              const float4 ww = w4[h4];
+              s0 = fmaf(ww.x, fmaxf(__uint_as_float(v[4 * h4 + 0]), 0.f), s0);
+              s1 = fmaf(ww.y, fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f), s1);
+              s2 = fmaf(ww.z, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f), s2);
+              s3 = fmaf(ww.w, fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f), s3);
+            }
+          } else {
+            // s < 0: s * min(x, 0) = |s| * max(-x, 0) = ReLU(s * x)
+#pragma unroll
+            for (int h4 = 0; h4 < kHeads / 4; ++h4) {
+              const float4 ww = w4[h4];
+              s0 = fmaf(ww.x, fminf(__uint_as_float(v[4 * h4 + 0]), 0.f), s0);
+              s1 = fmaf(ww.y, fminf(__uint_as_float(v[4 * h4 + 1]), 0.f), s1);
+              s2 = fmaf(ww.z, fminf(__uint_as_float(v[4 * h4 + 2]), 0.f), s2);
+              s3 = fmaf(ww.w, fminf(__uint_as_float(v[4 * h4 + 3]), 0.f), s3);
+            }
+          }
+          val[rr] = ((s0 + s1) + (s2 + s3)) * scale;
+        }
+        if (j < p.N) {
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr)
+            __stcs(orow[rr] + j, (j >= lo[rr] && j < hi[rr]) ? val[rr] : ninf);
+        }
+      }
+      if (!ok) {
+        raise_error(p.scratch, abort_flag, kErrTimeout);
+        break;
+      }
+      if (p.clean && (in.flags & 2)) {
+        for (int rr = 0; rr < 2; ++rr)
+          fill_neg_inf(orow[rr], in.t1 * kKeysPerTile, p.N, tid128);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+  if (threadIdx.x == 0) {
+    // Last CTA out resets the unit counter for the next call on this stream.
+    __threadfence();
+    const int prev = atomicAdd(p.scratch + 1, 1);
+    if (prev == static_cast<int>(gridDim.x) - 1) {
+      atomicExch(p.scratch + 0, 0);
+      atomicExch(p.scratch + 1, 0);
+      __threadfence();
+    }
+  }
+}
+
+}  // namespace dsa

@@ -1,0 +1,48 @@
+"""Parity comparison of the CUDA path against the float64 oracle.
+
+The bar: the -inf pattern is bit-exact on every compared row, every in-window
+value is finite, and in-window |gpu - ref| / (1e-6 + den) <= 2e-3 where
+den = sum_h |w_h| * |sm_scale * q_h . k| (the oracle's float64 value).
+"""
+import numpy as np
+
+import oracle
+
+REL_TOL = 2e-3
+
+
+def oracle_rows(case, rows=None, nthreads=0):
+    out, den, _ = oracle.logits(case.fmt, case.q, case.k, case.w, case.ks, case.ke,
+                                case.sm_scale, q_sf=case.q_sf, k_sf=case.k_sf,
+                                k_tok=case.k_tok, w_fmt=case.w_fmt, H=case.H, D=case.D,
+                                rows=rows, nthreads=nthreads)
+    return out, den
+
+
+def expected_mask(case, rows=None):
+    """True where the column lies outside row's clamped window [ks, ke)."""
+    ks = case.ks.reshape(-1).astype(np.int64)
+    ke = case.ke.reshape(-1).astype(np.int64)
+    if rows is not None:
+        ks, ke = ks[rows], ke[rows]
+    lo = np.clip(ks, 0, case.N)[:, None]
+    hi = np.clip(ke, 0, case.N)[:, None]
+    cols = np.arange(case.N)[None, :]
+    return (cols < lo) | (cols >= hi)
+
+
+def compare(gpu_rows, ref, den, *, check_outside=True, tol=REL_TOL):
+    """gpu_rows, ref, den: [R, N]. Returns the max relative error in-window."""
+    gpu = np.asarray(gpu_rows, dtype=np.float64)
+    ref_inf = np.isneginf(ref)
+    if check_outside:
+        got_inf = np.isneginf(gpu)
+        bad = np.argwhere(got_inf != ref_inf)
+        assert bad.size == 0, f"-inf pattern differs at {bad[:8].tolist()} (of {len(bad)})"
+    inside = ~ref_inf
+    g = gpu[inside]
+    assert np.all(np.isfinite(g)), "non-finite value inside the window"
+    rel = np.abs(g - ref[inside]) / (1e-6 + den[inside])
+    worst = float(rel.max()) if rel.size else 0.0
+    assert worst <= tol, f"max relative error {worst:.3e} > {tol}"
+    return worst

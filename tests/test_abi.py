@@ -1,0 +1,103 @@
+"""C-ABI checks that need no GPU: the library builds, loads, exports every
+symbol that include/dsa_indexer.h declares, and rejects bad arguments on the
+host before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from infra_dsa_indexer_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa_indexer.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"IDX_API\s+[\w\s\*]+?\b(indexer_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_api():
+    syms = declared_symbols()
+    assert "indexer_logits" in syms and "indexer_get_last_error" in syms
+    assert len(syms) >= 7
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        getattr(lib, name)
+
+
+def test_binding_exposes_same_names():
+    for name in declared_symbols():
+        assert callable(getattr(binding, name)), name
+
+
+def test_status_strings(lib):
+    for st in range(0, 10):
+        assert binding.indexer_status_string(st)
+    assert "unknown" in binding.indexer_status_string(12345)
+    assert binding.indexer_version() >= 100
+    assert binding.indexer_launches_per_call() >= 1
+
+
+FAKE = ctypes.c_void_p(0x1000)      # never dereferenced: validation fails first
+
+
+def call(lib, shape, **over):
+    args = dict(q=FAKE, q_sf=None, k=FAKE, k_sf=None, k_scales=None, w=FAKE, ks=FAKE, ke=FAKE,
+                sm_scale=ctypes.c_float(0.1), clean=1, out=FAKE)
+    args.update(over)
+    return lib.indexer_logits(args["q"], args["q_sf"], args["k"], args["k_sf"],
+                              args["k_scales"], args["w"], args["ks"], args["ke"],
+                              args["sm_scale"], args["clean"], args["out"],
+                              ctypes.byref(shape), None)
+
+
+def shp(**kw):
+    base = dict(B=1, S=8, N=100, H=64, D=128, fmt=0, w_fmt=0)
+    base.update(kw)
+    return binding.make_shape(**base)
+
+
+@pytest.mark.parametrize("over,shape_kw,status", [
+    (dict(q=None), {}, 1),
+    (dict(out=None), {}, 1),
+    ({}, dict(H=32), 2),
+    ({}, dict(D=64), 2),
+    ({}, dict(S=6), 2),
+    ({}, dict(N=0), 2),
+    ({}, dict(B=0), 2),
+    ({}, dict(out_row_stride=50), 2),
+    ({}, dict(fmt=7), 3),
+    ({}, dict(w_fmt=3), 3),
+    ({}, dict(fmt=2), 1),                                 # MX without scales
+    (dict(q_sf=FAKE, k_sf=FAKE), dict(fmt=0), 3),         # scales for a plain format
+    (dict(k_scales=FAKE), dict(fmt=0), 3),                # per-key scale only for E4M3
+    (dict(q=ctypes.c_void_p(0x1004)), {}, 4),             # misaligned base
+    ({}, dict(k_row_bytes=264), 4),                       # stride not a multiple of 16
+    (dict(sm_scale=ctypes.c_float(float("inf"))), {}, 5),
+    (dict(sm_scale=ctypes.c_float(float("nan"))), {}, 5),
+])
+def test_host_validation(lib, over, shape_kw, status):
+    assert call(lib, shp(**shape_kw), **over) == status
+
+
+def test_null_shape(lib):
+    assert lib.indexer_logits(FAKE, None, FAKE, None, None, FAKE, FAKE, FAKE,
+                              ctypes.c_float(1.0), 1, FAKE, None, None) == 1
+
+
+def test_binding_raises_without_cuda_tensors(lib):
+    import torch
+    t = torch.zeros(4)
+    with pytest.raises(ValueError):
+        binding.indexer_logits(t, None, t, None, None, t, t, t, 1.0, True, t, shp())
