@@ -64,7 +64,7 @@ typedef enum idx_status {
   IDX_ERR_SHAPE = 2,       /* H != 64, D != 128, S % 4 != 0, B/S < 1, N < 1,
                               out_row_stride < N, or a size beyond int32 indexing    */
   IDX_ERR_FORMAT = 3,      /* unknown fmt / w_fmt, or scales missing for MX          */
-  IDX_ERR_ALIGN = 4,       /* q/k base or row stride not 16-byte aligned              */
+  IDX_ERR_ALIGN = 4,       /* q/k/w base or q/k stride not 16-byte aligned             */
   IDX_ERR_SCALE = 5,       /* sm_scale is not finite                                  */
   IDX_ERR_DEVICE = 6,      /* current device is not compute capability 10.3 (sm_103) */
   IDX_ERR_CUDA = 7,        /* a CUDA runtime call failed (launch, allocation, ...)   */
@@ -102,7 +102,7 @@ typedef struct idx_shape {
  *  k_scales IDX_FMT_E4M3 only: FP32 [B,N] per-key scale >= 0 multiplying K
  *           (a per-query-row Q scale belongs in w); NULL means 1. Must be NULL
  *           for the other formats.
- *  w        [B,S,H] FP32 or BF16 (w_fmt), dense.
+ *  w        [B,S,H] FP32 or BF16 (w_fmt), dense, base 16-byte aligned.
  *  ks, ke   [B,S] int32, dense. Row (b,i) sees keys [max(ks,0), min(ke,N));
  *           ks >= ke is an empty row (all -inf). Values are clamped on the
  *           device; any int32 is accepted.

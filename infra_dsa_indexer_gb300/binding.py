@@ -145,7 +145,7 @@ def case_to_device(case, device="cuda", out_row_stride=None):
             return None
         if a.dtype == np.uint16:          # bf16 codes travel as int16 bit patterns
             a = a.view(np.int16)
-        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+        return torch.from_numpy(np.require(a, requirements=["C", "W"])).to(device)
     t = dict(q=dev(case.q), k=dev(case.k), w=dev(case.w), ks=dev(case.ks), ke=dev(case.ke),
              q_sf=dev(case.q_sf), k_sf=dev(case.k_sf), k_scales=dev(case.k_tok))
     stride = out_row_stride or case.N

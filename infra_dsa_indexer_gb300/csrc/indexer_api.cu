@@ -119,7 +119,7 @@ const char* indexer_status_string(int status) {
     case IDX_ERR_NULL: return "a required pointer is NULL";
     case IDX_ERR_SHAPE: return "unsupported or inconsistent shape (H must be 64, D 128, S % 4 == 0, N >= 1, out_row_stride >= N)";
     case IDX_ERR_FORMAT: return "unknown format, or scales missing/present for the wrong format";
-    case IDX_ERR_ALIGN: return "q/k base address or row stride is not 16-byte aligned";
+    case IDX_ERR_ALIGN: return "q/k/w base address or q/k stride is not 16-byte aligned";
     case IDX_ERR_SCALE: return "sm_scale is not finite";
     case IDX_ERR_DEVICE: return "current device is not compute capability 10.3 (sm_103)";
     case IDX_ERR_CUDA: return "a CUDA runtime call failed";
@@ -165,7 +165,8 @@ int indexer_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
   const int64_t total_rows = static_cast<int64_t>(sh.B) * sh.S;
   if (total_rows * sh.H >= (int64_t(1) << 31) || static_cast<int64_t>(sh.B) * sh.N >= (int64_t(1) << 31))
     return IDX_ERR_SHAPE;
-  if (!aligned16(q) || !aligned16(k) || q_row % 16 || k_row % 16 || k_batch % 16)
+  if (!aligned16(q) || !aligned16(k) || !aligned16(w) || q_row % 16 || k_row % 16 ||
+      k_batch % 16)
     return IDX_ERR_ALIGN;
   if (sh.fmt == IDX_FMT_MXFP8 || sh.fmt == IDX_FMT_MXFP4) return IDX_ERR_UNSUPPORTED;
 

@@ -22,17 +22,20 @@
 //    out through a global atomic counter, longest row-blocks first (for causal
 //    windows the highest row index), so the persistent grid balances itself.
 //
-// Roles (384 threads, one CTA per SM):
-//  warp 0       scheduler + TMA producer (one elected lane)
-//  warp 1       TMEM allocator + MMA issuer (one elected lane)
-//  warps 2-3    idle
-//  warps 4-11   epilogue: TMEM -> registers, ReLU.w head sum, masked FP32
-//               stores, -inf fill of columns outside the row-block's tiles.
-//               Warp w reads TMEM lanes 32*(w%4)..+31 (the sub-partition it
-//               may access); warps 4-7 own rows 0,1 of the block, 8-11 rows 2,3.
-// Pipelines (mbarriers): unit slots x2 (unit info + Q block), key-tile ring
-// (STAGES), TMEM accumulators x2 (2 x 256 columns), so the MMA of tile t+1
-// overlaps the epilogue of tile t.
+// Roles (640 threads = 20 warps, one CTA per SM):
+//  warp 0       K-tile TMA producer (one lane)
+//  warp 1       TMEM allocator + MMA issuer (one lane)
+//  warp 2       unit scheduler: fetches the next unit, its windows, and starts
+//               the TMA of its Q block and the bulk copy of its head weights,
+//               one unit ahead of the MMA (one lane)
+//  warp 3       idle
+//  warps 4-19   epilogue, one query row of the block per group of 4 warps:
+//               warp w reads TMEM lanes 32*(w%4)..+31 (the sub-partition it
+//               may access) of row (w-4)/4; TMEM -> registers, ReLU.w head
+//               sum, masked FP32 stores, -inf fill outside the block's tiles.
+// Pipelines (mbarriers): unit slots x2 (unit info + Q block + W), key-tile
+// ring (kStages), TMEM accumulators x2 (2 x 256 columns), so the MMA of tile
+// t+1 overlaps the epilogue of tile t.
 #pragma once
 #include <cuda.h>
 #include <cstdint>
@@ -46,10 +49,9 @@ constexpr int kRowsPerBlock = 4;
 constexpr int kHeads = 64;
 constexpr int kBlockN = kRowsPerBlock * kHeads;  // MMA N = 256
 constexpr int kHeadDim = 128;                    // MMA K per tile
-constexpr int kThreads = 384;
 constexpr int kEpiWarp0 = 4;
-constexpr int kNumEpiWarps = 8;
-constexpr int kNumEpiThreads = kNumEpiWarps * 32;
+constexpr int kNumEpiWarps = 16;
+constexpr int kThreads = (kEpiWarp0 + kNumEpiWarps) * 32;  // 640
 constexpr uint32_t kTmemCols = 512;
 
 enum : int { kFmtBF16 = 0, kFmtE4M3 = 1, kFmtMXFP8 = 2, kFmtMXFP4 = 3 };
@@ -108,7 +110,7 @@ struct Traits<kFmtE4M3> {
   static constexpr int kPanelElems = 128;
   static constexpr int kPanels = 1;
   static constexpr int kMmaK = 32;
-  static constexpr int kStages = 6;
+  static constexpr int kStages = 8;
   static constexpr uint32_t kIdesc = instr_desc(0, 0, kKeysPerTile, kBlockN);  // E4M3 x E4M3
   static constexpr int kKind = 1;
 };
@@ -121,14 +123,16 @@ struct Layout {
   static constexpr int kQPanelBytes = kBlockN * kPanelRowBytes;
   static constexpr int kKTileBytes = kKPanelBytes * T::kPanels;
   static constexpr int kQBlockBytes = kQPanelBytes * T::kPanels;
+  static constexpr int kWBytes = kRowsPerBlock * kHeads * 4;  // FP32 size; BF16 uses half
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + 2 * kQBlockBytes;
   static constexpr int kWOff = kKOff + T::kStages * kKTileBytes;
-  static constexpr int kInfoOff = kWOff + 2 * kRowsPerBlock * kHeads * 4;
+  static constexpr int kInfoOff = kWOff + 2 * kWBytes;
   static constexpr int kBarOff = kInfoOff + 2 * (int)sizeof(UnitInfo);
-  static constexpr int kNumBars = 2 + 2 + 2 * T::kStages + 2 + 2 + 2;
+  static constexpr int kNumBars = 2 + 2 + 2 * T::kStages + 2 + 2;
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
   static constexpr int kBytes = kMiscOff + 16;
+  static_assert(kBytes <= 232448, "shared memory budget");
 };
 
 __device__ __forceinline__ int clampi(int v, int lo, int hi) {
@@ -147,6 +151,75 @@ __device__ __forceinline__ void fill_neg_inf(float* row, int a, int b, int tid12
   for (int j = a + tid128; j < b; j += 128) __stcs(row + j, ninf);
 }
 
+// Accumulates sum_h w[h] * R(x[h]) over 32 heads of one row, R(x) = max(x, 0)
+// (NEG: min(x, 0)). Heads are taken in groups of four: two through max/min on
+// the ALU pipe, two through x + |x| = 2 max(x, 0) (x - |x| = 2 min(x, 0)) on
+// the FMA pipe, each pair then multiply-accumulated with one packed FP32x2
+// FMA, so the two pipes share the work. `am` collects the max/min half, `ad`
+// the doubled x +- |x| half; head_total() combines them. Weights come from
+// shared memory as FP32 or BF16 (`wrow` points at the first of the 32 heads).
+struct HeadAcc {
+  float2 am0, am1, ad0, ad1;
+};
+
+template <bool NEG, bool WBF16>
+__device__ __forceinline__ void head_reduce32(const uint32_t (&v)[32], const uint8_t* wrow,
+                                              HeadAcc& a) {
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    float4 w;
+    if constexpr (WBF16) {
+      const uint2 u = reinterpret_cast<const uint2*>(wrow)[g];
+      w = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                      __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+    } else {
+      w = reinterpret_cast<const float4*>(wrow)[g];
+    }
+    const float x0 = __uint_as_float(v[4 * g + 0]);
+    const float x1 = __uint_as_float(v[4 * g + 1]);
+    const float x2 = __uint_as_float(v[4 * g + 2]);
+    const float x3 = __uint_as_float(v[4 * g + 3]);
+    float2 rm, rd;
+    if constexpr (NEG) {
+      rm = make_float2(fminf(x0, 0.f), fminf(x1, 0.f));
+      rd = make_float2(x2 - fabsf(x2), x3 - fabsf(x3));
+    } else {
+      rm = make_float2(fmaxf(x0, 0.f), fmaxf(x1, 0.f));
+      rd = make_float2(x2 + fabsf(x2), x3 + fabsf(x3));
+    }
+    if (g & 1) {
+      a.am1 = __ffma2_rn(make_float2(w.x, w.y), rm, a.am1);
+      a.ad1 = __ffma2_rn(make_float2(w.z, w.w), rd, a.ad1);
+    } else {
+      a.am0 = __ffma2_rn(make_float2(w.x, w.y), rm, a.am0);
+      a.ad0 = __ffma2_rn(make_float2(w.z, w.w), rd, a.ad0);
+    }
+  }
+}
+
+__device__ __forceinline__ float head_total(const HeadAcc& a) {
+  const float sm = (a.am0.x + a.am0.y) + (a.am1.x + a.am1.y);
+  const float sd = (a.ad0.x + a.ad0.y) + (a.ad1.x + a.ad1.y);
+  return fmaf(sd, 0.5f, sm);
+}
+
+template <bool NEG, bool WBF16>
+__device__ __forceinline__ void head_half(const uint32_t (&v)[32], const uint8_t* wrow,
+                                          int half, HeadAcc& a) {
+  head_reduce32<NEG, WBF16>(v, wrow + half * 32 * (WBF16 ? 2 : 4), a);
+}
+
+__device__ __forceinline__ void head_half_rt(bool neg, bool wbf16, const uint32_t (&v)[32],
+                                             const uint8_t* wrow, int half, HeadAcc& a) {
+  if (wbf16) {
+    if (neg) head_half<true, true>(v, wrow, half, a);
+    else head_half<false, true>(v, wrow, half, a);
+  } else {
+    if (neg) head_half<true, false>(v, wrow, half, a);
+    else head_half<false, false>(v, wrow, half, a);
+  }
+}
+
 template <int FMT>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_logits_kernel(const __grid_constant__ KernelParams p) {
@@ -156,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   uint8_t* qbuf = smem + L::kQOff;
   uint8_t* kbuf = smem + L::kKOff;
-  float* w_s = reinterpret_cast<float*>(smem + L::kWOff);
+  uint8_t* wbuf = smem + L::kWOff;
   UnitInfo* info = reinterpret_cast<UnitInfo*>(smem + L::kInfoOff);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* unit_full = bars;
@@ -165,7 +238,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* k_empty = k_full + T::kStages;
   uint64_t* acc_full = k_empty + T::kStages;
   uint64_t* acc_empty = acc_full + 2;
-  uint64_t* w_ready = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
 
@@ -180,10 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     for (int s = 0; s < 2; ++s) {
       mbar_init(&unit_full[s], 1);
-      mbar_init(&unit_empty[s], 1 + kNumEpiWarps);
+      mbar_init(&unit_empty[s], 2 + kNumEpiWarps);  // K producer, MMA commit, epilogue warps
       mbar_init(&acc_full[s], 1);
       mbar_init(&acc_empty[s], kNumEpiWarps);
-      mbar_init(&w_ready[s], kNumEpiThreads);
     }
     for (int s = 0; s < T::kStages; ++s) {
       mbar_init(&k_full[s], 1);
@@ -200,14 +271,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const bool misaligned = (smem_u32(smem) & 1023u) != 0;
+  const uint32_t w_unit_bytes = p.w_bf16 ? L::kWBytes / 2 : L::kWBytes;
 
-  if (!misaligned && warp == 0 && lane == 0) {
-    // ---------------------------------------------------------------- producer
+  if (misaligned) {
+    // nothing: the error word says why
+  } else if (warp == 2 && lane == 0) {
+    // ---------------------------------------------------------- unit scheduler
     prefetch_tmap(&p.tmap_q);
-    prefetch_tmap(&p.tmap_k);
-    const uint64_t pol_k = policy_evict_last();   // K is re-read by every row-block
-    const uint64_t pol_q = policy_evict_first();  // Q block is read once per unit
-    uint32_t kiter = 0;
+    const uint64_t pol_first = policy_evict_first();  // Q block, W: read once per unit
     for (uint32_t it = 0;; ++it) {
       const int slot = it & 1;
       if (!mbar_wait(&unit_empty[slot], ((it >> 1) & 1) ^ 1, abort_flag, p.timeout_ns)) {
@@ -229,6 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = order % p.B;
       const int grow0 = b * p.S + blk * kRowsPerBlock;
       int lo_all = p.N, hi_all = 0;
+#pragma unroll
       for (int r = 0; r < kRowsPerBlock; ++r) {
         const int lo = clampi(__ldg(p.ks + grow0 + r), 0, p.N);
         const int hi = clampi(__ldg(p.ke + grow0 + r), 0, p.N);
@@ -245,8 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         t1 = (hi_all + kKeysPerTile - 1) / kKeysPerTile;
       }
       const int len = (t1 - t0 + p.nchunk - 1) / p.nchunk;
-      int c0 = min(t1, t0 + chunk * len);
-      int c1 = min(t1, c0 + len);
+      const int c0 = min(t1, t0 + chunk * len);
+      const int c1 = min(t1, c0 + len);
       in.stop = 0;
       in.b = b;
       in.grow0 = grow0;
@@ -255,15 +327,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       in.t0 = t0;
       in.t1 = t1;
       in.flags = (chunk == 0 ? 1 : 0) | (chunk == p.nchunk - 1 ? 2 : 0);
-      if (c1 > c0) {
-        mbar_arrive_expect_tx(&unit_full[slot], L::kQBlockBytes);
+      const bool has_tiles = c1 > c0;
+      mbar_arrive_expect_tx(&unit_full[slot], (has_tiles ? L::kQBlockBytes : 0) + w_unit_bytes);
+      if (has_tiles) {
         uint8_t* qdst = qbuf + slot * L::kQBlockBytes;
+#pragma unroll
         for (int pnl = 0; pnl < T::kPanels; ++pnl)
           tma_load_2d(qdst + pnl * L::kQPanelBytes, &p.tmap_q, &unit_full[slot],
-                      pnl * T::kPanelElems, grow0 * kHeads, pol_q);
-      } else {
-        mbar_arrive(&unit_full[slot]);
+                      pnl * T::kPanelElems, grow0 * kHeads, pol_first);
       }
+      const uint8_t* wsrc = reinterpret_cast<const uint8_t*>(p.w) +
+                            static_cast<int64_t>(grow0) * kHeads * (p.w_bf16 ? 2 : 4);
+      bulk_load(wbuf + slot * L::kWBytes, wsrc, w_unit_bytes, &unit_full[slot], pol_first);
+    }
+  } else if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------- K-tile producer
+    prefetch_tmap(&p.tmap_k);
+    const uint64_t pol_k = policy_evict_last();   // K is re-read by every row-block
+    uint32_t kiter = 0;
+    for (uint32_t it = 0;; ++it) {
+      const int slot = it & 1;
+      if (!mbar_wait(&unit_full[slot], (it >> 1) & 1, abort_flag, p.timeout_ns)) {
+        raise_error(p.scratch, abort_flag, kErrTimeout);
+        break;
+      }
+      const UnitInfo& in = info[slot];
+      if (in.stop) break;
+      const int c0 = in.c0, c1 = in.c1, b = in.b;
       bool ok = true;
       for (int t = c0; t < c1; ++t, ++kiter) {
         const int st = kiter % T::kStages;
@@ -274,6 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_arrive_expect_tx(&k_full[st], L::kKTileBytes);
         uint8_t* kdst = kbuf + st * L::kKTileBytes;
+#pragma unroll
         for (int pnl = 0; pnl < T::kPanels; ++pnl)
           tma_load_3d(kdst + pnl * L::kKPanelBytes, &p.tmap_k, &k_full[st],
                       pnl * T::kPanelElems, t * kKeysPerTile, b, pol_k);
@@ -282,8 +373,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         raise_error(p.scratch, abort_flag, kErrTimeout);
         break;
       }
+      mbar_arrive(&unit_empty[slot]);
     }
-  } else if (!misaligned && warp == 1 && lane == 0) {
+  } else if (warp == 1 && lane == 0) {
     // --------------------------------------------------------------- MMA issuer
     uint32_t kiter = 0, aiter = 0;
     for (uint32_t it = 0;; ++it) {
@@ -327,13 +419,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_commit(&unit_empty[slot]);
     }
-  } else if (!misaligned && warp >= kEpiWarp0) {
+  } else if (warp >= kEpiWarp0) {
     // ---------------------------------------------------------------- epilogue
-    const int ew = warp - kEpiWarp0;         // 0..7
-    const int et = threadIdx.x - kEpiWarp0 * 32;  // 0..255
-    const int quarter = warp & 3;            // TMEM sub-partition of this warp
-    const int pair = ew >> 2;                // rows 2*pair, 2*pair+1
-    const int tid128 = quarter * 32 + lane;  // index among the 4 warps of a pair
+    const int quarter = warp & 3;                // TMEM sub-partition of this warp
+    const int row = (warp - kEpiWarp0) >> 2;     // row of the block handled here
+    const int tid128 = quarter * 32 + lane;      // index among the row's 4 warps
     const bool neg = p.sm_scale < 0.f;
     const float ninf = __int_as_float(0xff800000);
     uint32_t aiter = 0;
@@ -343,105 +433,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         raise_error(p.scratch, abort_flag, kErrTimeout);
         break;
       }
-      const UnitInfo in = info[slot];
+      const UnitInfo& in = info[slot];
       if (in.stop) break;
-      // Stage this unit's head weights (4 rows x 64 heads) as FP32.
-      float* ws = w_s + slot * kRowsPerBlock * kHeads;
-      {
-        const int64_t widx = static_cast<int64_t>(in.grow0) * kHeads + et;
-        float wv;
-        if (p.w_bf16) {
-          const uint16_t bits = __ldg(reinterpret_cast<const uint16_t*>(p.w) + widx);
-          wv = __uint_as_float(static_cast<uint32_t>(bits) << 16);
-        } else {
-          wv = __ldg(reinterpret_cast<const float*>(p.w) + widx);
-        }
-        ws[et] = wv;
-      }
-      // All epilogue threads see all 256 weights (bounded wait, no named barrier).
-      mbar_arrive(&w_ready[slot]);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&unit_empty[slot]);
-      if (!mbar_wait(&w_ready[slot], (it >> 1) & 1, abort_flag, p.timeout_ns)) {
-        raise_error(p.scratch, abort_flag, kErrTimeout);
-        break;
-      }
-
-      const int r0 = 2 * pair;
-      float* orow[2];
-      int lo[2], hi[2];
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        orow[rr] = p.out + static_cast<int64_t>(in.grow0 + r0 + rr) * p.out_row_stride;
-        lo[rr] = in.lo[r0 + rr];
-        hi[rr] = in.hi[r0 + rr];
-      }
-      if (p.clean && (in.flags & 1)) {
-        for (int rr = 0; rr < 2; ++rr) fill_neg_inf(orow[rr], 0, in.t0 * kKeysPerTile, tid128);
-      }
+      const int b = in.b, c0 = in.c0, c1 = in.c1, t0 = in.t0, t1 = in.t1, flags = in.flags;
+      const int lo = in.lo[row], hi = in.hi[row];
+      float* orow = p.out + static_cast<int64_t>(in.grow0 + row) * p.out_row_stride;
+      const uint8_t* wrow = wbuf + slot * L::kWBytes + row * kHeads * (p.w_bf16 ? 2 : 4);
+      if (p.clean && (flags & 1)) fill_neg_inf(orow, 0, t0 * kKeysPerTile, tid128);
       bool ok = true;
-      for (int t = in.c0; t < in.c1; ++t, ++aiter) {
+      for (int t = c0; t < c1; ++t, ++aiter) {
         const int acc = aiter & 1;
+        const int j = t * kKeysPerTile + quarter * 32 + lane;
+        float scale = p.sm_scale;
+        if (FMT == kFmtE4M3 && p.k_scales != nullptr && j < p.N)
+          scale *= __ldg(p.k_scales + static_cast<int64_t>(b) * p.N + j);
         if (!mbar_wait(&acc_full[acc], (aiter >> 1) & 1, abort_flag, p.timeout_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const int j = t * kKeysPerTile + quarter * 32 + lane;
-        float scale = p.sm_scale;
-        if (FMT == kFmtE4M3 && p.k_scales != nullptr && j < p.N)
-          scale *= __ldg(p.k_scales + static_cast<int64_t>(in.b) * p.N + j);
-        float val[2];
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          uint32_t v[64];
-          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                 acc * kBlockN + (r0 + rr) * kHeads;
-          __syncwarp();  // tcgen05.ld is warp-collective: converge first
-          tmem_ld_64cols(taddr, v);
-          if (rr == 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[acc]);
-          }
-          const float4* w4 = reinterpret_cast<const float4*>(ws + (r0 + rr) * kHeads);
-          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-          if (!neg) {
-#pragma unroll
-            for (int h4 = 0; h4 < kHeads / 4; ++h4) {
-              const float4 ww = w4[h4];
-              s0 = fmaf(ww.x, fmaxf(__uint_as_float(v[4 * h4 + 0]), 0.f), s0);
-              s1 = fmaf(ww.y, fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f), s1);
-              s2 = fmaf(ww.z, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f), s2);
-              s3 = fmaf(ww.w, fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f), s3);
-            }
-          } else {
-            // s < 0: s * min(x, 0) = |s| * max(-x, 0) = ReLU(s * x)
-#pragma unroll
-            for (int h4 = 0; h4 < kHeads / 4; ++h4) {
-              const float4 ww = w4[h4];
-              s0 = fmaf(ww.x, fminf(__uint_as_float(v[4 * h4 + 0]), 0.f), s0);
-              s1 = fmaf(ww.y, fminf(__uint_as_float(v[4 * h4 + 1]), 0.f), s1);
-              s2 = fmaf(ww.z, fminf(__uint_as_float(v[4 * h4 + 2]), 0.f), s2);
-              s3 = fmaf(ww.w, fminf(__uint_as_float(v[4 * h4 + 3]), 0.f), s3);
-            }
-          }
-          val[rr] = ((s0 + s1) + (s2 + s3)) * scale;
-        }
-        if (j < p.N) {
-#pragma unroll
-          for (int rr = 0; rr < 2; ++rr)
-            __stcs(orow[rr] + j, (j >= lo[rr] && j < hi[rr]) ? val[rr] : ninf);
-        }
+        __syncwarp();  // tcgen05.ld is warp-collective: converge first
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                               acc * kBlockN + row * kHeads;
+        HeadAcc ha;
+        ha.am0 = ha.am1 = ha.ad0 = ha.ad1 = make_float2(0.f, 0.f);
+        uint32_t v[32];
+        tmem_ld_32cols(taddr, v);
+        head_half_rt(neg, p.w_bf16, v, wrow, 0, ha);
+        __syncwarp();
+        tmem_ld_32cols(taddr + 32, v);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        head_half_rt(neg, p.w_bf16, v, wrow, 1, ha);
+        const float sum = head_total(ha);
+        if (j < p.N) __stcs(orow + j, (j >= lo && j < hi) ? sum * scale : ninf);
       }
       if (!ok) {
         raise_error(p.scratch, abort_flag, kErrTimeout);
         break;
       }
-      if (p.clean && (in.flags & 2)) {
-        for (int rr = 0; rr < 2; ++rr)
-          fill_neg_inf(orow[rr], in.t1 * kKeysPerTile, p.N, tid128);
-      }
+      if (p.clean && (flags & 2)) fill_neg_inf(orow, t1 * kKeysPerTile, p.N, tid128);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&unit_empty[slot]);
     }
   }
 
