@@ -25,7 +25,7 @@ struct DeviceInfo {
   bool valid = false;
   int sm_count = 0;
   int cc_major = 0, cc_minor = 0;
-  bool smem_set[4] = {false, false, false, false};
+  bool smem_set[8] = {false, false, false, false, false, false, false, false};
 };
 
 std::mutex g_mutex;

@@ -151,73 +151,35 @@ __device__ __forceinline__ void fill_neg_inf(float* row, int a, int b, int tid12
   for (int j = a + tid128; j < b; j += 128) __stcs(row + j, ninf);
 }
 
-// Accumulates sum_h w[h] * R(x[h]) over 32 heads of one row, R(x) = max(x, 0)
-// (NEG: min(x, 0)). Heads are taken in groups of four: two through max/min on
-// the ALU pipe, two through x + |x| = 2 max(x, 0) (x - |x| = 2 min(x, 0)) on
-// the FMA pipe, each pair then multiply-accumulated with one packed FP32x2
-// FMA, so the two pipes share the work. `am` collects the max/min half, `ad`
-// the doubled x +- |x| half; head_total() combines them. Weights come from
-// shared memory as FP32 or BF16 (`wrow` points at the first of the 32 heads).
-struct HeadAcc {
-  float2 am0, am1, ad0, ad1;
-};
-
-template <bool NEG, bool WBF16>
-__device__ __forceinline__ void head_reduce32(const uint32_t (&v)[32], const uint8_t* wrow,
-                                              HeadAcc& a) {
+// sum_h w[h] * max(x[h], 0) over the 64 heads of one row. Heads are taken in
+// groups of four: two through max on the ALU pipe, two through x + |x| =
+// 2 max(x, 0) on the FMA pipe, each pair then multiply-accumulated with one
+// packed FP32x2 FMA, so both pipes share the work. The x + |x| half is
+// scaled by 1/2 at the end (exact). `w` is the row's 64 FP32 weights in
+// shared memory. A negative sm_scale never reaches this function: the MMA
+// negates its A operand instead (ReLU(s*x) = |s| * max(-x, 0)).
+__device__ __forceinline__ float head_reduce(const uint32_t (&v)[64], const float* w) {
+  float2 am0 = make_float2(0.f, 0.f), am1 = am0, ad0 = am0, ad1 = am0;
 #pragma unroll
-  for (int g = 0; g < 8; ++g) {
-    float4 w;
-    if constexpr (WBF16) {
-      const uint2 u = reinterpret_cast<const uint2*>(wrow)[g];
-      w = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
-                      __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
-    } else {
-      w = reinterpret_cast<const float4*>(wrow)[g];
-    }
+  for (int g = 0; g < kHeads / 4; ++g) {
+    const float4 ww = reinterpret_cast<const float4*>(w)[g];
     const float x0 = __uint_as_float(v[4 * g + 0]);
     const float x1 = __uint_as_float(v[4 * g + 1]);
     const float x2 = __uint_as_float(v[4 * g + 2]);
     const float x3 = __uint_as_float(v[4 * g + 3]);
-    float2 rm, rd;
-    if constexpr (NEG) {
-      rm = make_float2(fminf(x0, 0.f), fminf(x1, 0.f));
-      rd = make_float2(x2 - fabsf(x2), x3 - fabsf(x3));
-    } else {
-      rm = make_float2(fmaxf(x0, 0.f), fmaxf(x1, 0.f));
-      rd = make_float2(x2 + fabsf(x2), x3 + fabsf(x3));
-    }
+    const float2 rm = make_float2(fmaxf(x0, 0.f), fmaxf(x1, 0.f));
+    const float2 rd = make_float2(x2 + fabsf(x2), x3 + fabsf(x3));
     if (g & 1) {
-      a.am1 = __ffma2_rn(make_float2(w.x, w.y), rm, a.am1);
-      a.ad1 = __ffma2_rn(make_float2(w.z, w.w), rd, a.ad1);
+      am1 = __ffma2_rn(make_float2(ww.x, ww.y), rm, am1);
+      ad1 = __ffma2_rn(make_float2(ww.z, ww.w), rd, ad1);
     } else {
-      a.am0 = __ffma2_rn(make_float2(w.x, w.y), rm, a.am0);
-      a.ad0 = __ffma2_rn(make_float2(w.z, w.w), rd, a.ad0);
+      am0 = __ffma2_rn(make_float2(ww.x, ww.y), rm, am0);
+      ad0 = __ffma2_rn(make_float2(ww.z, ww.w), rd, ad0);
     }
   }
-}
-
-__device__ __forceinline__ float head_total(const HeadAcc& a) {
-  const float sm = (a.am0.x + a.am0.y) + (a.am1.x + a.am1.y);
-  const float sd = (a.ad0.x + a.ad0.y) + (a.ad1.x + a.ad1.y);
+  const float sm = (am0.x + am0.y) + (am1.x + am1.y);
+  const float sd = (ad0.x + ad0.y) + (ad1.x + ad1.y);
   return fmaf(sd, 0.5f, sm);
-}
-
-template <bool NEG, bool WBF16>
-__device__ __forceinline__ void head_half(const uint32_t (&v)[32], const uint8_t* wrow,
-                                          int half, HeadAcc& a) {
-  head_reduce32<NEG, WBF16>(v, wrow + half * 32 * (WBF16 ? 2 : 4), a);
-}
-
-__device__ __forceinline__ void head_half_rt(bool neg, bool wbf16, const uint32_t (&v)[32],
-                                             const uint8_t* wrow, int half, HeadAcc& a) {
-  if (wbf16) {
-    if (neg) head_half<true, true>(v, wrow, half, a);
-    else head_half<false, true>(v, wrow, half, a);
-  } else {
-    if (neg) head_half<true, false>(v, wrow, half, a);
-    else head_half<false, false>(v, wrow, half, a);
-  }
 }
 
 template <int FMT>
@@ -271,25 +233,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const bool misaligned = (smem_u32(smem) & 1023u) != 0;
-  const uint32_t w_unit_bytes = p.w_bf16 ? L::kWBytes / 2 : L::kWBytes;
 
   if (misaligned) {
     // nothing: the error word says why
-  } else if (warp == 2 && lane == 0) {
+  } else if (warp == 2) {
     // ---------------------------------------------------------- unit scheduler
-    prefetch_tmap(&p.tmap_q);
-    const uint64_t pol_first = policy_evict_first();  // Q block, W: read once per unit
+    // Lane 0 claims units, writes the unit info and starts the Q TMA; all 32
+    // lanes copy the block's head weights into shared memory as FP32.
+    if (lane == 0) prefetch_tmap(&p.tmap_q);
+    const uint64_t pol_first = policy_evict_first();  // Q block: read once per unit
     for (uint32_t it = 0;; ++it) {
       const int slot = it & 1;
-      if (!mbar_wait(&unit_empty[slot], ((it >> 1) & 1) ^ 1, abort_flag, p.timeout_ns)) {
-        raise_error(p.scratch, abort_flag, kErrTimeout);
+      int ok = 1, u = 0;
+      if (lane == 0) {
+        ok = mbar_wait(&unit_empty[slot], ((it >> 1) & 1) ^ 1, abort_flag, p.timeout_ns);
+        if (ok) u = atomicAdd(p.scratch + 0, 1);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      if (!ok) {
+        if (lane == 0) raise_error(p.scratch, abort_flag, kErrTimeout);
         break;
       }
-      const int u = atomicAdd(p.scratch + 0, 1);
       UnitInfo& in = info[slot];
       if (u >= p.num_units) {
-        in.stop = 1;
-        mbar_arrive(&unit_full[slot]);
+        if (lane == 0) {
+          in.stop = 1;
+          mbar_arrive(&unit_full[slot]);
+        }
         break;
       }
       // Units in order: row-blocks from the last (longest causal window) to
@@ -299,46 +270,67 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int blk = p.blocks_per_batch - 1 - order / p.B;
       const int b = order % p.B;
       const int grow0 = b * p.S + blk * kRowsPerBlock;
-      int lo_all = p.N, hi_all = 0;
+      // head weights of the 4 rows -> FP32 in shared memory
+      float* wdst = reinterpret_cast<float*>(wbuf + slot * L::kWBytes);
+      if (p.w_bf16) {
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.w) +
+                                static_cast<int64_t>(grow0) * (kHeads / 8) + lane);
+        const uint32_t r[4] = {raw.x, raw.y, raw.z, raw.w};
+        float4 lo4, hi4;
+        lo4 = make_float4(__uint_as_float(r[0] << 16), __uint_as_float(r[0] & 0xffff0000u),
+                          __uint_as_float(r[1] << 16), __uint_as_float(r[1] & 0xffff0000u));
+        hi4 = make_float4(__uint_as_float(r[2] << 16), __uint_as_float(r[2] & 0xffff0000u),
+                          __uint_as_float(r[3] << 16), __uint_as_float(r[3] & 0xffff0000u));
+        reinterpret_cast<float4*>(wdst)[2 * lane] = lo4;
+        reinterpret_cast<float4*>(wdst)[2 * lane + 1] = hi4;
+      } else {
+        const float4* src = reinterpret_cast<const float4*>(p.w) +
+                            static_cast<int64_t>(grow0) * (kHeads / 4);
+        reinterpret_cast<float4*>(wdst)[lane] = __ldg(src + lane);
+        reinterpret_cast<float4*>(wdst)[lane + 32] = __ldg(src + lane + 32);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        int lo_all = p.N, hi_all = 0;
 #pragma unroll
-      for (int r = 0; r < kRowsPerBlock; ++r) {
-        const int lo = clampi(__ldg(p.ks + grow0 + r), 0, p.N);
-        const int hi = clampi(__ldg(p.ke + grow0 + r), 0, p.N);
-        in.lo[r] = lo;
-        in.hi[r] = hi;
-        if (lo < hi) {
-          lo_all = min(lo_all, lo);
-          hi_all = max(hi_all, hi);
+        for (int r = 0; r < kRowsPerBlock; ++r) {
+          const int lo = clampi(__ldg(p.ks + grow0 + r), 0, p.N);
+          const int hi = clampi(__ldg(p.ke + grow0 + r), 0, p.N);
+          in.lo[r] = lo;
+          in.hi[r] = hi;
+          if (lo < hi) {
+            lo_all = min(lo_all, lo);
+            hi_all = max(hi_all, hi);
+          }
+        }
+        int t0 = 0, t1 = 0;
+        if (lo_all < hi_all) {
+          t0 = lo_all / kKeysPerTile;
+          t1 = (hi_all + kKeysPerTile - 1) / kKeysPerTile;
+        }
+        const int len = (t1 - t0 + p.nchunk - 1) / p.nchunk;
+        const int c0 = min(t1, t0 + chunk * len);
+        const int c1 = min(t1, c0 + len);
+        in.stop = 0;
+        in.b = b;
+        in.grow0 = grow0;
+        in.c0 = c0;
+        in.c1 = c1;
+        in.t0 = t0;
+        in.t1 = t1;
+        in.flags = (chunk == 0 ? 1 : 0) | (chunk == p.nchunk - 1 ? 2 : 0);
+        if (c1 > c0) {
+          mbar_arrive_expect_tx(&unit_full[slot], L::kQBlockBytes);
+          uint8_t* qdst = qbuf + slot * L::kQBlockBytes;
+#pragma unroll
+          for (int pnl = 0; pnl < T::kPanels; ++pnl)
+            tma_load_2d(qdst + pnl * L::kQPanelBytes, &p.tmap_q, &unit_full[slot],
+                        pnl * T::kPanelElems, grow0 * kHeads, pol_first);
+        } else {
+          mbar_arrive(&unit_full[slot]);
         }
       }
-      int t0 = 0, t1 = 0;
-      if (lo_all < hi_all) {
-        t0 = lo_all / kKeysPerTile;
-        t1 = (hi_all + kKeysPerTile - 1) / kKeysPerTile;
-      }
-      const int len = (t1 - t0 + p.nchunk - 1) / p.nchunk;
-      const int c0 = min(t1, t0 + chunk * len);
-      const int c1 = min(t1, c0 + len);
-      in.stop = 0;
-      in.b = b;
-      in.grow0 = grow0;
-      in.c0 = c0;
-      in.c1 = c1;
-      in.t0 = t0;
-      in.t1 = t1;
-      in.flags = (chunk == 0 ? 1 : 0) | (chunk == p.nchunk - 1 ? 2 : 0);
-      const bool has_tiles = c1 > c0;
-      mbar_arrive_expect_tx(&unit_full[slot], (has_tiles ? L::kQBlockBytes : 0) + w_unit_bytes);
-      if (has_tiles) {
-        uint8_t* qdst = qbuf + slot * L::kQBlockBytes;
-#pragma unroll
-        for (int pnl = 0; pnl < T::kPanels; ++pnl)
-          tma_load_2d(qdst + pnl * L::kQPanelBytes, &p.tmap_q, &unit_full[slot],
-                      pnl * T::kPanelElems, grow0 * kHeads, pol_first);
-      }
-      const uint8_t* wsrc = reinterpret_cast<const uint8_t*>(p.w) +
-                            static_cast<int64_t>(grow0) * kHeads * (p.w_bf16 ? 2 : 4);
-      bulk_load(wbuf + slot * L::kWBytes, wsrc, w_unit_bytes, &unit_full[slot], pol_first);
+      __syncwarp();
     }
   } else if (warp == 0 && lane == 0) {
     // ------------------------------------------------------- K-tile producer
@@ -378,6 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1 && lane == 0) {
     // --------------------------------------------------------------- MMA issuer
     uint32_t kiter = 0, aiter = 0;
+    // ReLU(s*x) = |s| * max(-x, 0) for s < 0: negate the A operand (bit 13).
+    const uint32_t idesc = T::kIdesc | (p.sm_scale < 0.f ? (1u << 13) : 0u);
     for (uint32_t it = 0;; ++it) {
       const int slot = it & 1;
       if (!mbar_wait(&unit_full[slot], (it >> 1) & 1, abort_flag, p.timeout_ns)) {
@@ -408,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t off = (kk % kStepsPerPanel) * kStepBytes;
           const uint64_t a_desc = smem_desc(k_addr + pnl * L::kKPanelBytes + off, 1024, 2);
           const uint64_t b_desc = smem_desc(q_addr + pnl * L::kQPanelBytes + off, 1024, 2);
-          tc_mma<T::kKind>(d_tmem, a_desc, b_desc, T::kIdesc, kk > 0 ? 1u : 0u);
+          tc_mma<T::kKind>(d_tmem, a_desc, b_desc, idesc, kk > 0 ? 1u : 0u);
         }
         tc_commit(&k_empty[st]);
         tc_commit(&acc_full[acc]);
@@ -424,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;                // TMEM sub-partition of this warp
     const int row = (warp - kEpiWarp0) >> 2;     // row of the block handled here
     const int tid128 = quarter * 32 + lane;      // index among the row's 4 warps
-    const bool neg = p.sm_scale < 0.f;
+    const float sm_abs = fabsf(p.sm_scale);
     const float ninf = __int_as_float(0xff800000);
     uint32_t aiter = 0;
     for (uint32_t it = 0;; ++it) {
@@ -438,13 +432,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = in.b, c0 = in.c0, c1 = in.c1, t0 = in.t0, t1 = in.t1, flags = in.flags;
       const int lo = in.lo[row], hi = in.hi[row];
       float* orow = p.out + static_cast<int64_t>(in.grow0 + row) * p.out_row_stride;
-      const uint8_t* wrow = wbuf + slot * L::kWBytes + row * kHeads * (p.w_bf16 ? 2 : 4);
+      const float* wrow = reinterpret_cast<const float*>(wbuf + slot * L::kWBytes) + row * kHeads;
       if (p.clean && (flags & 1)) fill_neg_inf(orow, 0, t0 * kKeysPerTile, tid128);
       bool ok = true;
       for (int t = c0; t < c1; ++t, ++aiter) {
         const int acc = aiter & 1;
         const int j = t * kKeysPerTile + quarter * 32 + lane;
-        float scale = p.sm_scale;
+        float scale = sm_abs;
         if (FMT == kFmtE4M3 && p.k_scales != nullptr && j < p.N)
           scale *= __ldg(p.k_scales + static_cast<int64_t>(b) * p.N + j);
         if (!mbar_wait(&acc_full[acc], (aiter >> 1) & 1, abort_flag, p.timeout_ns)) {
@@ -453,20 +447,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         __syncwarp();  // tcgen05.ld is warp-collective: converge first
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                               acc * kBlockN + row * kHeads;
-        HeadAcc ha;
-        ha.am0 = ha.am1 = ha.ad0 = ha.ad1 = make_float2(0.f, 0.f);
-        uint32_t v[32];
-        tmem_ld_32cols(taddr, v);
-        head_half_rt(neg, p.w_bf16, v, wrow, 0, ha);
-        __syncwarp();
-        tmem_ld_32cols(taddr + 32, v);
+        // Read the row's 64 columns, hand the accumulator back, then reduce.
+        uint32_t v[64];
+        tmem_ld_64cols(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kBlockN +
+                           row * kHeads,
+                       v);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[acc]);
-        head_half_rt(neg, p.w_bf16, v, wrow, 1, ha);
-        const float sum = head_total(ha);
+        const float sum = head_reduce(v, wrow);
         if (j < p.N) __stcs(orow + j, (j >= lo && j < hi) ? sum * scale : ninf);
       }
       if (!ok) {

@@ -77,6 +77,9 @@ def test_negative_and_zero_sm_scale():
     check_full(case)
     case = synth.make_case(synth.FMT_E4M3, 1, 8, 300, seed=6, windows="full", sm_scale=0.0)
     check_full(case)
+    case = synth.make_case(synth.FMT_E4M3, 2, 12, 700, seed=16, windows="causal",
+                           sm_scale=-0.125, w_fmt=synth.W_BF16)
+    check_full(case)
 
 
 def test_padded_output_rows_untouched_beyond_n():
