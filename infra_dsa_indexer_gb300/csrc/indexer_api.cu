@@ -101,7 +101,7 @@ int launch(const KernelParams& prm, int grid, DeviceInfo* di, cudaStream_t strea
       return IDX_ERR_CUDA;
     di->smem_set[FMT] = true;
   }
-  kern<<<grid, dsa::kThreads, smem, stream>>>(prm);
+  kern<<<grid, dsa::Layout<FMT>::kThreads, smem, stream>>>(prm);
   return cudaGetLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }
 

@@ -22,17 +22,22 @@
 //    out through a global atomic counter, longest row-blocks first (for causal
 //    windows the highest row index), so the persistent grid balances itself.
 //
-// Roles (640 threads = 20 warps, one CTA per SM):
+// Roles (one CTA per SM; 4 role warps + 8 or 16 epilogue warps):
 //  warp 0       K-tile TMA producer (one lane)
 //  warp 1       TMEM allocator + MMA issuer (one lane)
 //  warp 2       unit scheduler: fetches the next unit, its windows, and starts
 //               the TMA of its Q block and the bulk copy of its head weights,
 //               one unit ahead of the MMA (one lane)
 //  warp 3       idle
-//  warps 4-19   epilogue, one query row of the block per group of 4 warps:
-//               warp w reads TMEM lanes 32*(w%4)..+31 (the sub-partition it
-//               may access) of row (w-4)/4; TMEM -> registers, ReLU.w head
-//               sum, masked FP32 stores, -inf fill outside the block's tiles.
+//  warps 4..    epilogue, R = 1 or 2 query rows per warp (a per-format
+//               choice): warp w reads TMEM lanes 32*(w%4)..+31 (the
+//               sub-partition it may access) of rows R*((w-4)/4) .. +R-1; it
+//               loads its rows' accumulator columns, hands the buffer back to
+//               the MMA warp, then does the ReLU.w head sums, the masked FP32
+//               stores and the -inf fill outside the block's tiles. R = 2
+//               (8 warps, 170 registers each) suits BF16, where the MMA is
+//               long and the role warps need issue slots; R = 1 (16 warps)
+//               hides the epilogue's latency better when the MMA is short.
 // Pipelines (mbarriers): unit slots x2 (unit info + Q block + W), key-tile
 // ring (kStages), TMEM accumulators x2 (2 x 256 columns), so the MMA of tile
 // t+1 overlaps the epilogue of tile t.
@@ -50,8 +55,6 @@ constexpr int kHeads = 64;
 constexpr int kBlockN = kRowsPerBlock * kHeads;  // MMA N = 256
 constexpr int kHeadDim = 128;                    // MMA K per tile
 constexpr int kEpiWarp0 = 4;
-constexpr int kNumEpiWarps = 16;
-constexpr int kThreads = (kEpiWarp0 + kNumEpiWarps) * 32;  // 640
 constexpr uint32_t kTmemCols = 512;
 
 enum : int { kFmtBF16 = 0, kFmtE4M3 = 1, kFmtMXFP8 = 2, kFmtMXFP4 = 3 };
@@ -102,6 +105,7 @@ struct Traits<kFmtBF16> {
   static constexpr int kStages = 3;
   static constexpr uint32_t kIdesc = instr_desc(1, 1, kKeysPerTile, kBlockN);  // BF16 x BF16
   static constexpr int kKind = 0;
+  static constexpr int kRowsPerWarp = 2;
 };
 
 template <>
@@ -113,11 +117,14 @@ struct Traits<kFmtE4M3> {
   static constexpr int kStages = 8;
   static constexpr uint32_t kIdesc = instr_desc(0, 0, kKeysPerTile, kBlockN);  // E4M3 x E4M3
   static constexpr int kKind = 1;
+  static constexpr int kRowsPerWarp = 1;
 };
 
 template <int FMT>
 struct Layout {
   using T = Traits<FMT>;
+  static constexpr int kNumEpiWarps = 4 * kRowsPerBlock / T::kRowsPerWarp;
+  static constexpr int kThreads = (kEpiWarp0 + kNumEpiWarps) * 32;
   static constexpr int kPanelRowBytes = T::kRowBytes / T::kPanels;               // 128
   static constexpr int kKPanelBytes = kKeysPerTile * kPanelRowBytes;
   static constexpr int kQPanelBytes = kBlockN * kPanelRowBytes;
@@ -151,42 +158,61 @@ __device__ __forceinline__ void fill_neg_inf(float* row, int a, int b, int tid12
   for (int j = a + tid128; j < b; j += 128) __stcs(row + j, ninf);
 }
 
-// sum_h w[h] * max(x[h], 0) over the 64 heads of one row. Heads are taken in
-// groups of four: two through max on the ALU pipe, two through x + |x| =
-// 2 max(x, 0) on the FMA pipe, each pair then multiply-accumulated with one
-// packed FP32x2 FMA, so both pipes share the work. The x + |x| half is
-// scaled by 1/2 at the end (exact). `w` is the row's 64 FP32 weights in
-// shared memory. A negative sm_scale never reaches this function: the MMA
-// negates its A operand instead (ReLU(s*x) = |s| * max(-x, 0)).
-__device__ __forceinline__ float head_reduce(const uint32_t (&v)[64], const float* w) {
-  float2 am0 = make_float2(0.f, 0.f), am1 = am0, ad0 = am0, ad1 = am0;
-#pragma unroll
-  for (int g = 0; g < kHeads / 4; ++g) {
-    const float4 ww = reinterpret_cast<const float4*>(w)[g];
-    const float x0 = __uint_as_float(v[4 * g + 0]);
-    const float x1 = __uint_as_float(v[4 * g + 1]);
-    const float x2 = __uint_as_float(v[4 * g + 2]);
-    const float x3 = __uint_as_float(v[4 * g + 3]);
+// sum_h w[h] * max(x[h], 0) over the 64 heads of each of two rows (a, b),
+// interleaved for instruction-level parallelism. Heads are taken in groups of
+// four: two through max on the ALU pipe, two through x + |x| = 2 max(x, 0) on
+// the FMA pipe, each pair then multiply-accumulated with one packed FP32x2
+// FMA, so both pipes share the work. The x + |x| half is scaled by 1/2 at the
+// end (exact). `wa`, `wb` are the rows' 64 FP32 weights in shared memory. A
+// negative sm_scale never reaches this function: the MMA negates its A
+// operand instead (ReLU(s*x) = |s| * max(-x, 0)).
+struct RowAcc {
+  float2 m0, m1, d0, d1;
+  __device__ __forceinline__ void zero() { m0 = m1 = d0 = d1 = make_float2(0.f, 0.f); }
+  __device__ __forceinline__ void step(int g, float4 w, float x0, float x1, float x2, float x3) {
     const float2 rm = make_float2(fmaxf(x0, 0.f), fmaxf(x1, 0.f));
     const float2 rd = make_float2(x2 + fabsf(x2), x3 + fabsf(x3));
     if (g & 1) {
-      am1 = __ffma2_rn(make_float2(ww.x, ww.y), rm, am1);
-      ad1 = __ffma2_rn(make_float2(ww.z, ww.w), rd, ad1);
+      m1 = __ffma2_rn(make_float2(w.x, w.y), rm, m1);
+      d1 = __ffma2_rn(make_float2(w.z, w.w), rd, d1);
     } else {
-      am0 = __ffma2_rn(make_float2(ww.x, ww.y), rm, am0);
-      ad0 = __ffma2_rn(make_float2(ww.z, ww.w), rd, ad0);
+      m0 = __ffma2_rn(make_float2(w.x, w.y), rm, m0);
+      d0 = __ffma2_rn(make_float2(w.z, w.w), rd, d0);
     }
   }
-  const float sm = (am0.x + am0.y) + (am1.x + am1.y);
-  const float sd = (ad0.x + ad0.y) + (ad1.x + ad1.y);
-  return fmaf(sd, 0.5f, sm);
+  __device__ __forceinline__ float total() const {
+    const float sm = (m0.x + m0.y) + (m1.x + m1.y);
+    const float sd = (d0.x + d0.y) + (d1.x + d1.y);
+    return fmaf(sd, 0.5f, sm);
+  }
+};
+
+// R rows at once: v[r] holds row r's 64 accumulator columns, w + r*64 its weights.
+template <int R>
+__device__ __forceinline__ void head_reduce(const uint32_t (&v)[R][64], const float* w,
+                                            float (&out)[R]) {
+  RowAcc a[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) a[r].zero();
+#pragma unroll
+  for (int g = 0; g < kHeads / 4; ++g) {
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      a[r].step(g, reinterpret_cast<const float4*>(w + r * kHeads)[g], __uint_as_float(v[r][4 * g]),
+                __uint_as_float(v[r][4 * g + 1]), __uint_as_float(v[r][4 * g + 2]),
+                __uint_as_float(v[r][4 * g + 3]));
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) out[r] = a[r].total();
 }
 
 template <int FMT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
     indexer_logits_kernel(const __grid_constant__ KernelParams p) {
   using T = Traits<FMT>;
   using L = Layout<FMT>;
+  constexpr int kNumEpiWarps = L::kNumEpiWarps;
+  constexpr int R = T::kRowsPerWarp;
   extern __shared__ __align__(1024) uint8_t smem[];
 
   uint8_t* qbuf = smem + L::kQOff;
@@ -372,6 +398,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t kiter = 0, aiter = 0;
     // ReLU(s*x) = |s| * max(-x, 0) for s < 0: negate the A operand (bit 13).
     const uint32_t idesc = T::kIdesc | (p.sm_scale < 0.f ? (1u << 13) : 0u);
+    // K-major, 128-byte swizzle, 8-row groups 1024 bytes apart.
+    const uint64_t k_desc0 = smem_desc(smem_u32(kbuf), 1024, 2);
+    const uint64_t q_desc0 = smem_desc(smem_u32(qbuf), 1024, 2);
     for (uint32_t it = 0;; ++it) {
       const int slot = it & 1;
       if (!mbar_wait(&unit_full[slot], (it >> 1) & 1, abort_flag, p.timeout_ns)) {
@@ -381,31 +410,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       const UnitInfo& in = info[slot];
       if (in.stop) break;
       const int c0 = in.c0, c1 = in.c1;
-      const uint32_t q_addr = smem_u32(qbuf + slot * L::kQBlockBytes);
+      const uint64_t b_base = q_desc0 + ((slot * L::kQBlockBytes) >> 4);
       bool ok = true;
+      bool ready = false;  // barriers of tile t already seen complete
       for (int t = c0; t < c1; ++t, ++kiter, ++aiter) {
         const int st = kiter % T::kStages;
         const int acc = aiter & 1;
-        if (!mbar_wait(&k_full[st], (kiter / T::kStages) & 1, abort_flag, p.timeout_ns) ||
-            !mbar_wait(&acc_empty[acc], ((aiter >> 1) & 1) ^ 1, abort_flag, p.timeout_ns)) {
+        if (!ready &&
+            (!mbar_wait(&k_full[st], (kiter / T::kStages) & 1, abort_flag, p.timeout_ns) ||
+             !mbar_wait(&acc_empty[acc], ((aiter >> 1) & 1) ^ 1, abort_flag, p.timeout_ns))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t k_addr = smem_u32(kbuf + st * L::kKTileBytes);
+        // Descriptors differ only in the start-address field (bits 0-13,
+        // address >> 4), so every step is the stage/slot base plus an offset.
+        const uint64_t a_base = k_desc0 + ((st * L::kKTileBytes) >> 4);
         const uint32_t d_tmem = tmem_base + acc * kBlockN;
+        // The next tile's barriers are polled (non-blocking) between MMA
+        // issues: an issue waits for room in the tensor pipe, so the polls
+        // ride under execution instead of idling the pipe after the tile.
+        const bool has_next = t + 1 < c1;
+        const uint32_t nst = (kiter + 1) % T::kStages, npar = ((kiter + 1) / T::kStages) & 1;
+        const uint32_t nacc = (aiter + 1) & 1, napar = (((aiter + 1) >> 1) & 1) ^ 1;
+        bool next_k = !has_next, next_a = !has_next;
         constexpr int kStepsPerPanel = T::kPanelElems / T::kMmaK;
         constexpr int kStepBytes = T::kMmaK * (T::kRowBytes / kHeadDim);  // 32 B
 #pragma unroll
         for (int kk = 0; kk < T::kPanels * kStepsPerPanel; ++kk) {
-          const int pnl = kk / kStepsPerPanel;
-          const uint32_t off = (kk % kStepsPerPanel) * kStepBytes;
-          const uint64_t a_desc = smem_desc(k_addr + pnl * L::kKPanelBytes + off, 1024, 2);
-          const uint64_t b_desc = smem_desc(q_addr + pnl * L::kQPanelBytes + off, 1024, 2);
-          tc_mma<T::kKind>(d_tmem, a_desc, b_desc, idesc, kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk / kStepsPerPanel) * L::kKPanelBytes + (kk % kStepsPerPanel) * kStepBytes;
+          const uint32_t offq = (kk / kStepsPerPanel) * L::kQPanelBytes + (kk % kStepsPerPanel) * kStepBytes;
+          tc_mma<T::kKind>(d_tmem, a_base + (off >> 4), b_base + (offq >> 4), idesc,
+                           kk > 0 ? 1u : 0u);
+          if (!next_k) next_k = mbar_test(&k_full[nst], npar);
+          if (!next_a) next_a = mbar_test(&acc_empty[nacc], napar);
         }
         tc_commit(&k_empty[st]);
         tc_commit(&acc_full[acc]);
+        ready = has_next && next_k && next_a;
       }
       if (!ok) {
         raise_error(p.scratch, abort_flag, kErrTimeout);
@@ -415,9 +457,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kEpiWarp0) {
     // ---------------------------------------------------------------- epilogue
-    const int quarter = warp & 3;                // TMEM sub-partition of this warp
-    const int row = (warp - kEpiWarp0) >> 2;     // row of the block handled here
-    const int tid128 = quarter * 32 + lane;      // index among the row's 4 warps
+    const int quarter = warp & 3;                  // TMEM sub-partition of this warp
+    const int r0 = R * ((warp - kEpiWarp0) >> 2);  // rows r0 .. r0 + R - 1 of the block
+    const int tid128 = quarter * 32 + lane;        // index among the rows' 4 warps
     const float sm_abs = fabsf(p.sm_scale);
     const float ninf = __int_as_float(0xff800000);
     uint32_t aiter = 0;
@@ -430,10 +472,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const UnitInfo& in = info[slot];
       if (in.stop) break;
       const int b = in.b, c0 = in.c0, c1 = in.c1, t0 = in.t0, t1 = in.t1, flags = in.flags;
-      const int lo = in.lo[row], hi = in.hi[row];
-      float* orow = p.out + static_cast<int64_t>(in.grow0 + row) * p.out_row_stride;
-      const float* wrow = reinterpret_cast<const float*>(wbuf + slot * L::kWBytes) + row * kHeads;
-      if (p.clean && (flags & 1)) fill_neg_inf(orow, 0, t0 * kKeysPerTile, tid128);
+      int lo[R], hi[R];
+      float* orow[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        lo[r] = in.lo[r0 + r];
+        hi[r] = in.hi[r0 + r];
+        orow[r] = p.out + static_cast<int64_t>(in.grow0 + r0 + r) * p.out_row_stride;
+      }
+      const float* wrows = reinterpret_cast<const float*>(wbuf + slot * L::kWBytes) + r0 * kHeads;
+      if (p.clean && (flags & 1)) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) fill_neg_inf(orow[r], 0, t0 * kKeysPerTile, tid128);
+      }
       bool ok = true;
       for (int t = c0; t < c1; ++t, ++aiter) {
         const int acc = aiter & 1;
@@ -447,22 +498,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         __syncwarp();  // tcgen05.ld is warp-collective: converge first
-        // Read the row's 64 columns, hand the accumulator back, then reduce.
-        uint32_t v[64];
-        tmem_ld_64cols(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kBlockN +
-                           row * kHeads,
-                       v);
+        // Read the rows' 64 columns each, hand the accumulator back, reduce.
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                               acc * kBlockN + r0 * kHeads;
+        uint32_t v[R][64];
+#pragma unroll
+        for (int r = 0; r < R; ++r) tmem_ld_64cols(taddr + r * kHeads, v[r]);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[acc]);
-        const float sum = head_reduce(v, wrow);
-        if (j < p.N) __stcs(orow + j, (j >= lo && j < hi) ? sum * scale : ninf);
+        float sums[R];
+        head_reduce<R>(v, wrows, sums);
+        if (j < p.N) {
+#pragma unroll
+          for (int r = 0; r < R; ++r)
+            __stcs(orow[r] + j, (j >= lo[r] && j < hi[r]) ? sums[r] * scale : ninf);
+        }
       }
       if (!ok) {
         raise_error(p.scratch, abort_flag, kErrTimeout);
         break;
       }
-      if (p.clean && (flags & 2)) fill_neg_inf(orow, t1 * kKeysPerTile, p.N, tid128);
+      if (p.clean && (flags & 2)) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) fill_neg_inf(orow[r], t1 * kKeysPerTile, p.N, tid128);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&unit_empty[slot]);
     }
