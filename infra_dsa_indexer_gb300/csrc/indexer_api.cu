@@ -81,25 +81,27 @@ int get_scratch(int dev, cudaStream_t stream, int32_t** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// 2-D or 3-D tiled map with 128-byte swizzle. dims/strides in elements/bytes.
+// 2-D or 3-D tiled map. dims/strides in elements/bytes.
 int encode_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int rank,
-               const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box) {
+               const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+               CUtensorMapSwizzle swizzle) {
   uint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(map, dtype, rank, const_cast<void*>(base), dims, strides_bytes, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? IDX_OK : IDX_ERR_CUDA;
 }
 
-template <int FMT>
+template <int FMT, bool NEG_EPI>
 int launch(const KernelParams& prm, int grid, DeviceInfo* di, cudaStream_t stream) {
   constexpr int smem = dsa::Layout<FMT>::kBytes;
-  auto kern = dsa::indexer_logits_kernel<FMT>;
-  if (!di->smem_set[FMT]) {
+  auto kern = dsa::indexer_logits_kernel<FMT, NEG_EPI>;
+  bool& attr_set = di->smem_set[FMT * 2 + (NEG_EPI ? 1 : 0)];
+  if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
       return IDX_ERR_CUDA;
-    di->smem_set[FMT] = true;
+    attr_set = true;
   }
   kern<<<grid, dsa::Layout<FMT>::kThreads, smem, stream>>>(prm);
   return cudaGetLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
@@ -168,7 +170,8 @@ int indexer_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
   if (!aligned16(q) || !aligned16(k) || !aligned16(w) || q_row % 16 || k_row % 16 ||
       k_batch % 16)
     return IDX_ERR_ALIGN;
-  if (sh.fmt == IDX_FMT_MXFP8 || sh.fmt == IDX_FMT_MXFP4) return IDX_ERR_UNSUPPORTED;
+  if (mx && ((reinterpret_cast<uintptr_t>(q_sf) & 3u) || (reinterpret_cast<uintptr_t>(k_sf) & 3u)))
+    return IDX_ERR_ALIGN;
 
   std::lock_guard<std::mutex> lock(g_mutex);
   int dev = 0;
@@ -185,19 +188,22 @@ int indexer_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
   std::memset(&prm, 0, sizeof(prm));
   const CUtensorMapDataType dt =
       sh.fmt == IDX_FMT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  const uint32_t panel_elems = sh.fmt == IDX_FMT_BF16 ? 64 : 128;
+  // One box spans one swizzle panel: 128 bytes (64-byte for packed E2M1 rows).
+  const bool fp4 = sh.fmt == IDX_FMT_MXFP4;
+  const uint32_t panel_elems = sh.fmt == IDX_FMT_BF16 ? 64 : (fp4 ? 64 : 128);
+  const CUtensorMapSwizzle swz = fp4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+  const uint64_t row_elems = fp4 ? static_cast<uint64_t>(sh.D / 2) : static_cast<uint64_t>(sh.D);
   {
-    const uint64_t dims[2] = {static_cast<uint64_t>(sh.D), static_cast<uint64_t>(total_rows * sh.H)};
+    const uint64_t dims[2] = {row_elems, static_cast<uint64_t>(total_rows * sh.H)};
     const uint64_t strides[1] = {static_cast<uint64_t>(q_row)};
     const uint32_t box[2] = {panel_elems, static_cast<uint32_t>(dsa::kBlockN)};
-    if ((st = encode_map(&prm.tmap_q, q, dt, 2, dims, strides, box))) return st;
+    if ((st = encode_map(&prm.tmap_q, q, dt, 2, dims, strides, box, swz))) return st;
   }
   {
-    const uint64_t dims[3] = {static_cast<uint64_t>(sh.D), static_cast<uint64_t>(sh.N),
-                              static_cast<uint64_t>(sh.B)};
+    const uint64_t dims[3] = {row_elems, static_cast<uint64_t>(sh.N), static_cast<uint64_t>(sh.B)};
     const uint64_t strides[2] = {static_cast<uint64_t>(k_row), static_cast<uint64_t>(k_batch)};
     const uint32_t box[3] = {panel_elems, static_cast<uint32_t>(dsa::kKeysPerTile), 1};
-    if ((st = encode_map(&prm.tmap_k, k, dt, 3, dims, strides, box))) return st;
+    if ((st = encode_map(&prm.tmap_k, k, dt, 3, dims, strides, box, swz))) return st;
   }
   prm.q_sf = q_sf;
   prm.k_sf = k_sf;
@@ -233,8 +239,12 @@ int indexer_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
   const int grid = static_cast<int>(std::min<int64_t>(di->sm_count, units));
 
   switch (sh.fmt) {
-    case IDX_FMT_BF16: return launch<dsa::kFmtBF16>(prm, grid, di, stream);
-    case IDX_FMT_E4M3: return launch<dsa::kFmtE4M3>(prm, grid, di, stream);
+    case IDX_FMT_BF16: return launch<dsa::kFmtBF16, false>(prm, grid, di, stream);
+    case IDX_FMT_E4M3: return launch<dsa::kFmtE4M3, false>(prm, grid, di, stream);
+    case IDX_FMT_MXFP8: return launch<dsa::kFmtMXFP8, false>(prm, grid, di, stream);
+    case IDX_FMT_MXFP4:
+      return sm_scale < 0.f ? launch<dsa::kFmtMXFP4, true>(prm, grid, di, stream)
+                            : launch<dsa::kFmtMXFP4, false>(prm, grid, di, stream);
     default: return IDX_ERR_UNSUPPORTED;
   }
 }

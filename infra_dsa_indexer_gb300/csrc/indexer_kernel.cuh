@@ -18,16 +18,22 @@
 //    K = D = 128. The FP32 accumulator lands in TMEM with one key per lane and
 //    one (row, head) per column, so the head reduction sum_h w*ReLU(s*x) is a
 //    per-thread loop over columns: no shuffles, no shared-memory reduction.
+//  * Kinds: BF16 kind::f16; E4M3 kind::f8f6f4; MXFP8 kind::mxf8f6f4 and MXFP4
+//    kind::mxf4, block-scaled with one E8M0 scale per 32 elements of D held in
+//    TMEM next to the accumulator.
 //  * A unit of work is (row-block, chunk of its key tiles). Units are handed
 //    out through a global atomic counter, longest row-blocks first (for causal
 //    windows the highest row index), so the persistent grid balances itself.
 //
 // Roles (one CTA per SM; 4 role warps + 8 or 16 epilogue warps):
-//  warp 0       K-tile TMA producer (one lane)
+//  warp 0       K-tile TMA producer (lane 0); for MX formats all 32 lanes also
+//               copy the tile's key scale factors into shared memory in the
+//               transposed order the TMEM copy wants (4-byte cp.async each)
 //  warp 1       TMEM allocator + MMA issuer (one lane)
-//  warp 2       unit scheduler: fetches the next unit, its windows, and starts
-//               the TMA of its Q block and the bulk copy of its head weights,
-//               one unit ahead of the MMA (one lane)
+//  warp 2       unit scheduler: claims the next unit, reads its windows, stages
+//               its head weights in shared memory as FP32 (and, for MX, its Q
+//               scale factors), and starts the TMA of its Q block, one unit
+//               ahead of the MMA
 //  warp 3       idle
 //  warps 4..    epilogue, R = 1 or 2 query rows per warp (a per-format
 //               choice): warp w reads TMEM lanes 32*(w%4)..+31 (the
@@ -38,9 +44,10 @@
 //               (8 warps, 170 registers each) suits BF16, where the MMA is
 //               long and the role warps need issue slots; R = 1 (16 warps)
 //               hides the epilogue's latency better when the MMA is short.
-// Pipelines (mbarriers): unit slots x2 (unit info + Q block + W), key-tile
-// ring (kStages), TMEM accumulators x2 (2 x 256 columns), so the MMA of tile
-// t+1 overlaps the epilogue of tile t.
+// Pipelines (mbarriers): unit slots x2 (unit info + Q block + W [+ Q scales]),
+// key-tile ring (kStages) [+ key scales], TMEM accumulators: two 256-column
+// buffers, or one for the MX formats (their scale factors use the rest), so
+// the MMA of tile t+1 overlaps the epilogue of tile t.
 #pragma once
 #include <cuda.h>
 #include <cstdint>
@@ -56,6 +63,11 @@ constexpr int kBlockN = kRowsPerBlock * kHeads;  // MMA N = 256
 constexpr int kHeadDim = 128;                    // MMA K per tile
 constexpr int kEpiWarp0 = 4;
 constexpr uint32_t kTmemCols = 512;
+constexpr int kStepBytes = 32;                   // bytes of K per MMA instruction
+constexpr uint32_t kSfaCol = 256;                // MX: key scale factors (4 columns)
+constexpr uint32_t kSfbCol = 260;                // MX: Q scale factors (8 columns)
+constexpr int kSfaBytes = kKeysPerTile * 4;      // one 32-bit word (4 E8M0) per key
+constexpr int kSfbBytes = kBlockN * 4;           // one word per (row, head)
 
 enum : int { kFmtBF16 = 0, kFmtE4M3 = 1, kFmtMXFP8 = 2, kFmtMXFP4 = 3 };
 enum : int { kErrTimeout = 8, kErrAlign = 4 };
@@ -93,31 +105,65 @@ struct KernelParams {
   uint64_t timeout_ns;
 };
 
+// Per-format constants. kRowBytes: bytes of one D=128 row of Q or K; the
+// operands are K-major with a swizzle of kSwizzleBytes (TMA writes the same
+// pattern), kPanels column panels of kSwizzleBytes each.
 template <int FMT>
 struct Traits;
 
 template <>
 struct Traits<kFmtBF16> {
-  static constexpr int kRowBytes = kHeadDim * 2;        // 256 B per key / head row
-  static constexpr int kPanelElems = 64;                // 128-byte swizzle span
-  static constexpr int kPanels = 2;
-  static constexpr int kMmaK = 16;
+  static constexpr int kRowBytes = kHeadDim * 2;
+  static constexpr int kSwizzleBytes = 128;
+  static constexpr int kTmaElemBytes = 2;
   static constexpr int kStages = 3;
   static constexpr uint32_t kIdesc = instr_desc(1, 1, kKeysPerTile, kBlockN);  // BF16 x BF16
   static constexpr int kKind = 0;
   static constexpr int kRowsPerWarp = 2;
+  static constexpr bool kMX = false;
+  static constexpr int kSfIdStep = 0;
 };
 
 template <>
 struct Traits<kFmtE4M3> {
   static constexpr int kRowBytes = kHeadDim;
-  static constexpr int kPanelElems = 128;
-  static constexpr int kPanels = 1;
-  static constexpr int kMmaK = 32;
+  static constexpr int kSwizzleBytes = 128;
+  static constexpr int kTmaElemBytes = 1;
   static constexpr int kStages = 8;
   static constexpr uint32_t kIdesc = instr_desc(0, 0, kKeysPerTile, kBlockN);  // E4M3 x E4M3
   static constexpr int kKind = 1;
   static constexpr int kRowsPerWarp = 1;
+  static constexpr bool kMX = false;
+  static constexpr int kSfIdStep = 0;
+};
+
+template <>
+struct Traits<kFmtMXFP8> {
+  static constexpr int kRowBytes = kHeadDim;
+  static constexpr int kSwizzleBytes = 128;
+  static constexpr int kTmaElemBytes = 1;
+  static constexpr int kStages = 8;
+  // E4M3 x E4M3, UE8M0 scales, one per 32 elements: MMA step kk (K = 32) uses
+  // scale byte kk of each row's 32-bit scale word.
+  static constexpr uint32_t kIdesc = instr_desc_bs(0, 0, kKeysPerTile, kBlockN, 0, 0);
+  static constexpr int kKind = 2;
+  static constexpr int kRowsPerWarp = 1;
+  static constexpr bool kMX = true;
+  static constexpr int kSfIdStep = 1;
+};
+
+template <>
+struct Traits<kFmtMXFP4> {
+  static constexpr int kRowBytes = kHeadDim / 2;  // two E2M1 per byte
+  static constexpr int kSwizzleBytes = 64;
+  static constexpr int kTmaElemBytes = 1;           // the tensor map walks bytes
+  static constexpr int kStages = 12;
+  // E2M1 x E2M1, UE8M0 scales: MMA step kk (K = 64) uses scale bytes 2kk, 2kk+1.
+  static constexpr uint32_t kIdesc = instr_desc_bs(1, 1, kKeysPerTile, kBlockN, 0, 0);
+  static constexpr int kKind = 3;
+  static constexpr int kRowsPerWarp = 1;
+  static constexpr bool kMX = true;
+  static constexpr int kSfIdStep = 2;
 };
 
 template <int FMT>
@@ -125,18 +171,24 @@ struct Layout {
   using T = Traits<FMT>;
   static constexpr int kNumEpiWarps = 4 * kRowsPerBlock / T::kRowsPerWarp;
   static constexpr int kThreads = (kEpiWarp0 + kNumEpiWarps) * 32;
-  static constexpr int kPanelRowBytes = T::kRowBytes / T::kPanels;               // 128
-  static constexpr int kKPanelBytes = kKeysPerTile * kPanelRowBytes;
-  static constexpr int kQPanelBytes = kBlockN * kPanelRowBytes;
-  static constexpr int kKTileBytes = kKPanelBytes * T::kPanels;
-  static constexpr int kQBlockBytes = kQPanelBytes * T::kPanels;
-  static constexpr int kWBytes = kRowsPerBlock * kHeads * 4;  // FP32 size; BF16 uses half
+  static constexpr int kAccBufs = T::kMX ? 1 : 2;
+  static constexpr int kPanels = T::kRowBytes / T::kSwizzleBytes;
+  static constexpr int kSteps = T::kRowBytes / kStepBytes;           // MMAs per tile
+  static constexpr int kStepsPerPanel = T::kSwizzleBytes / kStepBytes;
+  static constexpr int kAtomBytes = 8 * T::kSwizzleBytes;            // 8-row swizzle atom
+  static constexpr int kKPanelBytes = kKeysPerTile * T::kSwizzleBytes;
+  static constexpr int kQPanelBytes = kBlockN * T::kSwizzleBytes;
+  static constexpr int kKTileBytes = kKPanelBytes * kPanels;
+  static constexpr int kQBlockBytes = kQPanelBytes * kPanels;
+  static constexpr int kWBytes = kRowsPerBlock * kHeads * 4;  // FP32 weights of a block
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + 2 * kQBlockBytes;
   static constexpr int kWOff = kKOff + T::kStages * kKTileBytes;
-  static constexpr int kInfoOff = kWOff + 2 * kWBytes;
+  static constexpr int kSfaOff = kWOff + 2 * kWBytes;
+  static constexpr int kSfbOff = kSfaOff + (T::kMX ? T::kStages * kSfaBytes : 0);
+  static constexpr int kInfoOff = kSfbOff + (T::kMX ? 2 * kSfbBytes : 0);
   static constexpr int kBarOff = kInfoOff + 2 * (int)sizeof(UnitInfo);
-  static constexpr int kNumBars = 2 + 2 + 2 * T::kStages + 2 + 2;
+  static constexpr int kNumBars = 2 + 2 + 2 * T::kStages + 2 * kAccBufs + (T::kMX ? T::kStages : 0);
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
   static constexpr int kBytes = kMiscOff + 16;
   static_assert(kBytes <= 232448, "shared memory budget");
@@ -158,20 +210,25 @@ __device__ __forceinline__ void fill_neg_inf(float* row, int a, int b, int tid12
   for (int j = a + tid128; j < b; j += 128) __stcs(row + j, ninf);
 }
 
-// sum_h w[h] * max(x[h], 0) over the 64 heads of each of two rows (a, b),
-// interleaved for instruction-level parallelism. Heads are taken in groups of
-// four: two through max on the ALU pipe, two through x + |x| = 2 max(x, 0) on
-// the FMA pipe, each pair then multiply-accumulated with one packed FP32x2
-// FMA, so both pipes share the work. The x + |x| half is scaled by 1/2 at the
-// end (exact). `wa`, `wb` are the rows' 64 FP32 weights in shared memory. A
-// negative sm_scale never reaches this function: the MMA negates its A
-// operand instead (ReLU(s*x) = |s| * max(-x, 0)).
+// sum_h w[h] * R(x[h]) over the 64 heads of a row, R(x) = max(x, 0) (NEG:
+// min(x, 0)). Heads are taken in groups of four: two through max/min on the
+// ALU pipe, two through x + |x| = 2 max(x, 0) (x - |x| = 2 min(x, 0)) on the
+// FMA pipe, each pair then multiply-accumulated with one packed FP32x2 FMA,
+// so both pipes share the work. The doubled half is scaled by 1/2 at the end
+// (exact). NEG is used only where the MMA cannot negate its A operand.
+template <bool NEG>
 struct RowAcc {
   float2 m0, m1, d0, d1;
   __device__ __forceinline__ void zero() { m0 = m1 = d0 = d1 = make_float2(0.f, 0.f); }
   __device__ __forceinline__ void step(int g, float4 w, float x0, float x1, float x2, float x3) {
-    const float2 rm = make_float2(fmaxf(x0, 0.f), fmaxf(x1, 0.f));
-    const float2 rd = make_float2(x2 + fabsf(x2), x3 + fabsf(x3));
+    float2 rm, rd;
+    if constexpr (NEG) {
+      rm = make_float2(fminf(x0, 0.f), fminf(x1, 0.f));
+      rd = make_float2(x2 - fabsf(x2), x3 - fabsf(x3));
+    } else {
+      rm = make_float2(fmaxf(x0, 0.f), fmaxf(x1, 0.f));
+      rd = make_float2(x2 + fabsf(x2), x3 + fabsf(x3));
+    }
     if (g & 1) {
       m1 = __ffma2_rn(make_float2(w.x, w.y), rm, m1);
       d1 = __ffma2_rn(make_float2(w.z, w.w), rd, d1);
@@ -187,11 +244,12 @@ struct RowAcc {
   }
 };
 
-// R rows at once: v[r] holds row r's 64 accumulator columns, w + r*64 its weights.
-template <int R>
+// R rows at once: v[r] holds row r's 64 accumulator columns, w + r*64 its
+// 64 FP32 weights in shared memory. Rows are interleaved for ILP.
+template <int R, bool NEG>
 __device__ __forceinline__ void head_reduce(const uint32_t (&v)[R][64], const float* w,
                                             float (&out)[R]) {
-  RowAcc a[R];
+  RowAcc<NEG> a[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) a[r].zero();
 #pragma unroll
@@ -206,18 +264,36 @@ __device__ __forceinline__ void head_reduce(const uint32_t (&v)[R][64], const fl
   for (int r = 0; r < R; ++r) out[r] = a[r].total();
 }
 
-template <int FMT>
+template <int KIND>
+__device__ __forceinline__ void mma_step(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate, uint32_t sfa,
+                                         uint32_t sfb) {
+  if constexpr (KIND == 2) {
+    tc_mma_mxf8f6f4(d_tmem, a_desc, b_desc, idesc, sfa, sfb, accumulate);
+  } else if constexpr (KIND == 3) {
+    tc_mma_mxf4(d_tmem, a_desc, b_desc, idesc, sfa, sfb, accumulate);
+  } else {
+    tc_mma<KIND>(d_tmem, a_desc, b_desc, idesc, accumulate);
+  }
+}
+
+// NEG_EPI: the epilogue applies a negative sm_scale itself (MXFP4, whose MMA
+// kind has no negate bit); every other case negates the MMA's A operand.
+template <int FMT, bool NEG_EPI>
 __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
     indexer_logits_kernel(const __grid_constant__ KernelParams p) {
   using T = Traits<FMT>;
   using L = Layout<FMT>;
   constexpr int kNumEpiWarps = L::kNumEpiWarps;
+  constexpr int kAccBufs = L::kAccBufs;
   constexpr int R = T::kRowsPerWarp;
   extern __shared__ __align__(1024) uint8_t smem[];
 
   uint8_t* qbuf = smem + L::kQOff;
   uint8_t* kbuf = smem + L::kKOff;
   uint8_t* wbuf = smem + L::kWOff;
+  uint8_t* sfa_s = smem + L::kSfaOff;  // [kStages][128 keys x 4 bytes], TMEM-copy order
+  uint8_t* sfb_s = smem + L::kSfbOff;  // [2 slots][256 rows x 4 bytes], TMEM-copy order
   UnitInfo* info = reinterpret_cast<UnitInfo*>(smem + L::kInfoOff);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* unit_full = bars;
@@ -225,7 +301,8 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
   uint64_t* k_full = bars + 4;
   uint64_t* k_empty = k_full + T::kStages;
   uint64_t* acc_full = k_empty + T::kStages;
-  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* acc_empty = acc_full + kAccBufs;
+  uint64_t* sf_full = acc_empty + kAccBufs;  // MX only
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
 
@@ -234,19 +311,23 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     if ((smem_u32(smem) & 1023u) != 0) {
-      // The 128-byte swizzle atoms need a 1024-byte aligned base.
+      // The swizzle atoms need a 1024-byte aligned base.
       atomicExch(p.scratch + 2, kErrAlign);
     }
     *abort_flag = 0;
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&unit_full[s], 1);
+      // unit_full: the scheduler's arrive (+ one cp.async arrival per lane for MX)
+      mbar_init(&unit_full[s], T::kMX ? 1 + 32 : 1);
       mbar_init(&unit_empty[s], 2 + kNumEpiWarps);  // K producer, MMA commit, epilogue warps
+    }
+    for (int s = 0; s < kAccBufs; ++s) {
       mbar_init(&acc_full[s], 1);
       mbar_init(&acc_empty[s], kNumEpiWarps);
     }
     for (int s = 0; s < T::kStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
+      if constexpr (T::kMX) mbar_init(&sf_full[s], 32);
     }
     fence_mbar_init();
   }
@@ -265,7 +346,8 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
   } else if (warp == 2) {
     // ---------------------------------------------------------- unit scheduler
     // Lane 0 claims units, writes the unit info and starts the Q TMA; all 32
-    // lanes copy the block's head weights into shared memory as FP32.
+    // lanes copy the block's head weights into shared memory as FP32 and, for
+    // MX formats, its Q scale factors in TMEM-copy order.
     if (lane == 0) prefetch_tmap(&p.tmap_q);
     const uint64_t pol_first = policy_evict_first();  // Q block: read once per unit
     for (uint32_t it = 0;; ++it) {
@@ -287,6 +369,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
           in.stop = 1;
           mbar_arrive(&unit_full[slot]);
         }
+        if constexpr (T::kMX) cp_async_arrive(&unit_full[slot]);
         break;
       }
       // Units in order: row-blocks from the last (longest causal window) to
@@ -302,18 +385,30 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.w) +
                                 static_cast<int64_t>(grow0) * (kHeads / 8) + lane);
         const uint32_t r[4] = {raw.x, raw.y, raw.z, raw.w};
-        float4 lo4, hi4;
-        lo4 = make_float4(__uint_as_float(r[0] << 16), __uint_as_float(r[0] & 0xffff0000u),
-                          __uint_as_float(r[1] << 16), __uint_as_float(r[1] & 0xffff0000u));
-        hi4 = make_float4(__uint_as_float(r[2] << 16), __uint_as_float(r[2] & 0xffff0000u),
-                          __uint_as_float(r[3] << 16), __uint_as_float(r[3] & 0xffff0000u));
-        reinterpret_cast<float4*>(wdst)[2 * lane] = lo4;
-        reinterpret_cast<float4*>(wdst)[2 * lane + 1] = hi4;
+        reinterpret_cast<float4*>(wdst)[2 * lane] =
+            make_float4(__uint_as_float(r[0] << 16), __uint_as_float(r[0] & 0xffff0000u),
+                        __uint_as_float(r[1] << 16), __uint_as_float(r[1] & 0xffff0000u));
+        reinterpret_cast<float4*>(wdst)[2 * lane + 1] =
+            make_float4(__uint_as_float(r[2] << 16), __uint_as_float(r[2] & 0xffff0000u),
+                        __uint_as_float(r[3] << 16), __uint_as_float(r[3] & 0xffff0000u));
       } else {
         const float4* src = reinterpret_cast<const float4*>(p.w) +
                             static_cast<int64_t>(grow0) * (kHeads / 4);
         reinterpret_cast<float4*>(wdst)[lane] = __ldg(src + lane);
         reinterpret_cast<float4*>(wdst)[lane + 32] = __ldg(src + lane + 32);
+      }
+      if constexpr (T::kMX) {
+        // Q scale word of (row, head) m = 32c + lane goes to TMEM lane m % 32,
+        // column m / 32: in shared memory, chunk m / 128 (one TMEM copy
+        // each), row m % 32 (16 bytes), word (m % 128) / 32.
+        const uint8_t* src = p.q_sf + static_cast<int64_t>(grow0) * kHeads * 4;
+        uint8_t* dst = sfb_s + slot * kSfbBytes;
+#pragma unroll
+        for (int c = 0; c < kBlockN / 32; ++c) {
+          const int m = 32 * c + lane;
+          cp_async_4(dst + (m >> 7) * 512 + 16 * lane + 4 * (c & 3), src + 4 * m);
+        }
+        cp_async_arrive(&unit_full[slot]);
       }
       __syncwarp();
       if (lane == 0) {
@@ -349,58 +444,83 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
           mbar_arrive_expect_tx(&unit_full[slot], L::kQBlockBytes);
           uint8_t* qdst = qbuf + slot * L::kQBlockBytes;
 #pragma unroll
-          for (int pnl = 0; pnl < T::kPanels; ++pnl)
+          for (int pnl = 0; pnl < L::kPanels; ++pnl)
             tma_load_2d(qdst + pnl * L::kQPanelBytes, &p.tmap_q, &unit_full[slot],
-                        pnl * T::kPanelElems, grow0 * kHeads, pol_first);
+                        pnl * (T::kSwizzleBytes / T::kTmaElemBytes), grow0 * kHeads, pol_first);
         } else {
           mbar_arrive(&unit_full[slot]);
         }
       }
       __syncwarp();
     }
-  } else if (warp == 0 && lane == 0) {
+  } else if (warp == 0 && (T::kMX || lane == 0)) {
     // ------------------------------------------------------- K-tile producer
-    prefetch_tmap(&p.tmap_k);
-    const uint64_t pol_k = policy_evict_last();   // K is re-read by every row-block
+    // Lane 0 waits and issues the TMA; for MX formats all lanes also copy the
+    // tile's 128 key scale words (word of key m = 32c + lane to row `lane`,
+    // word c of the 16-byte rows the TMEM copy reads).
+    if (lane == 0) prefetch_tmap(&p.tmap_k);
+    const uint64_t pol_k = policy_evict_last();  // K is re-read by every row-block
     uint32_t kiter = 0;
     for (uint32_t it = 0;; ++it) {
       const int slot = it & 1;
-      if (!mbar_wait(&unit_full[slot], (it >> 1) & 1, abort_flag, p.timeout_ns)) {
-        raise_error(p.scratch, abort_flag, kErrTimeout);
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&unit_full[slot], (it >> 1) & 1, abort_flag, p.timeout_ns);
+      if constexpr (T::kMX) {
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        __syncwarp();  // lane 0's acquire covers the unit info the other lanes read
+      }
+      if (!ok) {
+        if (lane == 0) raise_error(p.scratch, abort_flag, kErrTimeout);
         break;
       }
       const UnitInfo& in = info[slot];
       if (in.stop) break;
       const int c0 = in.c0, c1 = in.c1, b = in.b;
-      bool ok = true;
       for (int t = c0; t < c1; ++t, ++kiter) {
         const int st = kiter % T::kStages;
-        if (!mbar_wait(&k_empty[st], ((kiter / T::kStages) & 1) ^ 1, abort_flag,
-                       p.timeout_ns)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&k_full[st], L::kKTileBytes);
-        uint8_t* kdst = kbuf + st * L::kKTileBytes;
+        if (lane == 0)
+          ok = mbar_wait(&k_empty[st], ((kiter / T::kStages) & 1) ^ 1, abort_flag, p.timeout_ns);
+        if constexpr (T::kMX) ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&k_full[st], L::kKTileBytes);
+          uint8_t* kdst = kbuf + st * L::kKTileBytes;
 #pragma unroll
-        for (int pnl = 0; pnl < T::kPanels; ++pnl)
-          tma_load_3d(kdst + pnl * L::kKPanelBytes, &p.tmap_k, &k_full[st],
-                      pnl * T::kPanelElems, t * kKeysPerTile, b, pol_k);
+          for (int pnl = 0; pnl < L::kPanels; ++pnl)
+            tma_load_3d(kdst + pnl * L::kKPanelBytes, &p.tmap_k, &k_full[st],
+                        pnl * (T::kSwizzleBytes / T::kTmaElemBytes), t * kKeysPerTile, b, pol_k);
+        }
+        if constexpr (T::kMX) {
+          uint8_t* dst = sfa_s + st * kSfaBytes + 16 * lane;
+          const uint8_t* src = p.k_sf + (static_cast<int64_t>(b) * p.N + t * kKeysPerTile) * 4;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int m = 32 * c + lane;
+            if (t * kKeysPerTile + m < p.N) cp_async_4(dst + 4 * c, src + 4 * m);
+          }
+          cp_async_arrive(&sf_full[st]);
+        }
       }
       if (!ok) {
-        raise_error(p.scratch, abort_flag, kErrTimeout);
+        if (lane == 0) raise_error(p.scratch, abort_flag, kErrTimeout);
         break;
       }
-      mbar_arrive(&unit_empty[slot]);
+      if (lane == 0) mbar_arrive(&unit_empty[slot]);
     }
   } else if (warp == 1 && lane == 0) {
     // --------------------------------------------------------------- MMA issuer
     uint32_t kiter = 0, aiter = 0;
-    // ReLU(s*x) = |s| * max(-x, 0) for s < 0: negate the A operand (bit 13).
-    const uint32_t idesc = T::kIdesc | (p.sm_scale < 0.f ? (1u << 13) : 0u);
-    // K-major, 128-byte swizzle, 8-row groups 1024 bytes apart.
-    const uint64_t k_desc0 = smem_desc(smem_u32(kbuf), 1024, 2);
-    const uint64_t q_desc0 = smem_desc(smem_u32(qbuf), 1024, 2);
+    // ReLU(s*x) = |s| * max(-x, 0) for s < 0: negate the A operand (bit 13),
+    // except where the epilogue applies the sign (NEG_EPI).
+    const uint32_t idesc = T::kIdesc | (!NEG_EPI && p.sm_scale < 0.f ? (1u << 13) : 0u);
+    // K-major operands, 8-row groups one swizzle atom apart; layout code
+    // 2 = 128-byte swizzle, 4 = 64-byte swizzle.
+    constexpr uint32_t kLayout = T::kSwizzleBytes == 128 ? 2u : 4u;
+    const uint64_t k_desc0 = smem_desc(smem_u32(kbuf), L::kAtomBytes, kLayout);
+    const uint64_t q_desc0 = smem_desc(smem_u32(qbuf), L::kAtomBytes, kLayout);
+    // Scale factors: 32 rows x 16 bytes, no swizzle, 8-row groups 128 bytes apart.
+    const uint64_t sfa_desc0 = smem_desc(smem_u32(sfa_s), 128, 0);
+    const uint64_t sfb_desc0 = smem_desc(smem_u32(sfb_s), 128, 0);
     for (uint32_t it = 0;; ++it) {
       const int slot = it & 1;
       if (!mbar_wait(&unit_full[slot], (it >> 1) & 1, abort_flag, p.timeout_ns)) {
@@ -415,14 +535,35 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       bool ready = false;  // barriers of tile t already seen complete
       for (int t = c0; t < c1; ++t, ++kiter, ++aiter) {
         const int st = kiter % T::kStages;
-        const int acc = aiter & 1;
-        if (!ready &&
-            (!mbar_wait(&k_full[st], (kiter / T::kStages) & 1, abort_flag, p.timeout_ns) ||
-             !mbar_wait(&acc_empty[acc], ((aiter >> 1) & 1) ^ 1, abort_flag, p.timeout_ns))) {
-          ok = false;
-          break;
+        const int acc = aiter % kAccBufs;
+        const uint32_t kpar = (kiter / T::kStages) & 1;
+        if (!ready) {
+          if (!mbar_wait(&k_full[st], kpar, abort_flag, p.timeout_ns) ||
+              (T::kMX && !mbar_wait(&sf_full[st], kpar, abort_flag, p.timeout_ns)) ||
+              !mbar_wait(&acc_empty[acc], ((aiter / kAccBufs) & 1) ^ 1, abort_flag,
+                         p.timeout_ns)) {
+            ok = false;
+            break;
+          }
         }
         tc_fence_after();
+        uint32_t sfa = 0, sfb = 0;
+        if constexpr (T::kMX) {
+          // The scale words were written by cp.async (generic proxy); the
+          // TMEM copy reads them through the async proxy. The copies run in
+          // issue order ahead of the MMAs below; one TMEM copy of each kind
+          // is in flight at a time because every tile waits for the
+          // accumulator, i.e. for the previous tile's MMAs to finish.
+          fence_proxy_async_smem();
+          sfa = tmem_base + kSfaCol;
+          sfb = tmem_base + kSfbCol;
+          if (t == c0) {
+            const uint64_t d = sfb_desc0 + ((slot * kSfbBytes) >> 4);
+            tc_cp_32x128b_warpx4(sfb, d);
+            tc_cp_32x128b_warpx4(sfb + 4, d + (512 >> 4));
+          }
+          tc_cp_32x128b_warpx4(sfa, sfa_desc0 + ((st * kSfaBytes) >> 4));
+        }
         // Descriptors differ only in the start-address field (bits 0-13,
         // address >> 4), so every step is the stage/slot base plus an offset.
         const uint64_t a_base = k_desc0 + ((st * L::kKTileBytes) >> 4);
@@ -432,22 +573,27 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         // ride under execution instead of idling the pipe after the tile.
         const bool has_next = t + 1 < c1;
         const uint32_t nst = (kiter + 1) % T::kStages, npar = ((kiter + 1) / T::kStages) & 1;
-        const uint32_t nacc = (aiter + 1) & 1, napar = (((aiter + 1) >> 1) & 1) ^ 1;
-        bool next_k = !has_next, next_a = !has_next;
-        constexpr int kStepsPerPanel = T::kPanelElems / T::kMmaK;
-        constexpr int kStepBytes = T::kMmaK * (T::kRowBytes / kHeadDim);  // 32 B
+        const uint32_t nacc = (aiter + 1) % kAccBufs;
+        const uint32_t napar = (((aiter + 1) / kAccBufs) & 1) ^ 1;
+        bool next_k = !has_next, next_s = !has_next || !T::kMX, next_a = !has_next;
 #pragma unroll
-        for (int kk = 0; kk < T::kPanels * kStepsPerPanel; ++kk) {
-          const uint32_t off = (kk / kStepsPerPanel) * L::kKPanelBytes + (kk % kStepsPerPanel) * kStepBytes;
-          const uint32_t offq = (kk / kStepsPerPanel) * L::kQPanelBytes + (kk % kStepsPerPanel) * kStepBytes;
-          tc_mma<T::kKind>(d_tmem, a_base + (off >> 4), b_base + (offq >> 4), idesc,
-                           kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < L::kSteps; ++kk) {
+          const uint32_t pnl = kk / L::kStepsPerPanel, step = kk % L::kStepsPerPanel;
+          const uint32_t off = pnl * L::kKPanelBytes + step * kStepBytes;
+          const uint32_t offq = pnl * L::kQPanelBytes + step * kStepBytes;
+          const uint32_t sf_id = kk * T::kSfIdStep;
+          const uint32_t id = T::kMX ? (idesc | (sf_id << 4) | (sf_id << 29)) : idesc;
+          mma_step<T::kKind>(d_tmem, a_base + (off >> 4), b_base + (offq >> 4), id,
+                             kk > 0 ? 1u : 0u, sfa, sfb);
           if (!next_k) next_k = mbar_test(&k_full[nst], npar);
+          if constexpr (T::kMX) {
+            if (!next_s) next_s = mbar_test(&sf_full[nst], npar);
+          }
           if (!next_a) next_a = mbar_test(&acc_empty[nacc], napar);
         }
         tc_commit(&k_empty[st]);
         tc_commit(&acc_full[acc]);
-        ready = has_next && next_k && next_a;
+        ready = has_next && next_k && next_s && next_a;
       }
       if (!ok) {
         raise_error(p.scratch, abort_flag, kErrTimeout);
@@ -460,7 +606,9 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
     const int quarter = warp & 3;                  // TMEM sub-partition of this warp
     const int r0 = R * ((warp - kEpiWarp0) >> 2);  // rows r0 .. r0 + R - 1 of the block
     const int tid128 = quarter * 32 + lane;        // index among the rows' 4 warps
-    const float sm_abs = fabsf(p.sm_scale);
+    // The MMA delivers x = s_sign * q.k (negated A for s < 0), so the sum is
+    // scaled by |s|; with NEG_EPI the epilogue sums min(x, 0) and scales by s.
+    const float sm_abs = NEG_EPI ? p.sm_scale : fabsf(p.sm_scale);
     const float ninf = __int_as_float(0xff800000);
     uint32_t aiter = 0;
     for (uint32_t it = 0;; ++it) {
@@ -487,12 +635,12 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       }
       bool ok = true;
       for (int t = c0; t < c1; ++t, ++aiter) {
-        const int acc = aiter & 1;
+        const int acc = aiter % kAccBufs;
         const int j = t * kKeysPerTile + quarter * 32 + lane;
         float scale = sm_abs;
         if (FMT == kFmtE4M3 && p.k_scales != nullptr && j < p.N)
           scale *= __ldg(p.k_scales + static_cast<int64_t>(b) * p.N + j);
-        if (!mbar_wait(&acc_full[acc], (aiter >> 1) & 1, abort_flag, p.timeout_ns)) {
+        if (!mbar_wait(&acc_full[acc], (aiter / kAccBufs) & 1, abort_flag, p.timeout_ns)) {
           ok = false;
           break;
         }
@@ -508,7 +656,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[acc]);
         float sums[R];
-        head_reduce<R>(v, wrows, sums);
+        head_reduce<R, NEG_EPI>(v, wrows, sums);
         if (j < p.N) {
 #pragma unroll
           for (int r = 0; r < R; ++r)

@@ -126,6 +126,20 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
+// 4-byte asynchronous copy global -> shared (non-bulk); any destination
+// address, so a copy loop can transpose while it moves data.
+__device__ __forceinline__ void cp_async_4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+
+// Arrive on `bar` once all cp.async copies this thread issued so far have
+// landed; the arrival is one of the barrier's expected arrivals (.noinc).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
 // Make generic-proxy shared-memory writes visible to the async proxy
 // (tcgen05.cp / tcgen05.mma operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -42,15 +42,16 @@ def check_full(case, **kw):
 
 
 PLAIN = [synth.FMT_BF16, synth.FMT_E4M3]
+ALL = [synth.FMT_BF16, synth.FMT_E4M3, synth.FMT_MXFP8, synth.FMT_MXFP4]
 
 
-@pytest.mark.parametrize("fmt", PLAIN)
+@pytest.mark.parametrize("fmt", ALL)
 def test_tiny_causal_workload(fmt):
     case = synth.make_workload("tiny_causal_bf16", fmt=fmt)
     check_full(case)
 
 
-@pytest.mark.parametrize("fmt", PLAIN)
+@pytest.mark.parametrize("fmt", ALL)
 @pytest.mark.parametrize("w_fmt", [synth.W_F32, synth.W_BF16])
 def test_random_windows_ragged(fmt, w_fmt):
     rng = np.random.default_rng(100 + fmt)
@@ -65,10 +66,9 @@ def test_random_windows_ragged(fmt, w_fmt):
 
 
 @pytest.mark.parametrize("N", [1, 127, 129, 999])
-def test_ragged_key_tails(N):
-    case = synth.make_case(synth.FMT_BF16, 1, 16, N, seed=N, windows="full")
-    check_full(case)
-    case = synth.make_case(synth.FMT_E4M3, 1, 16, N, seed=N + 1, windows="causal")
+@pytest.mark.parametrize("fmt", ALL)
+def test_ragged_key_tails(N, fmt):
+    case = synth.make_case(fmt, 1, 16, N, seed=N + fmt, windows="full" if fmt % 2 else "causal")
     check_full(case)
 
 
@@ -80,6 +80,9 @@ def test_negative_and_zero_sm_scale():
     case = synth.make_case(synth.FMT_E4M3, 2, 12, 700, seed=16, windows="causal",
                            sm_scale=-0.125, w_fmt=synth.W_BF16)
     check_full(case)
+    for fmt in (synth.FMT_MXFP8, synth.FMT_MXFP4):
+        case = synth.make_case(fmt, 1, 12, 400, seed=17 + fmt, windows="causal", sm_scale=-0.1)
+        check_full(case)
 
 
 def test_padded_output_rows_untouched_beyond_n():
@@ -98,7 +101,7 @@ def test_clean_false_in_window_values():
     compare(out.reshape(-1, 700), ref, den, check_outside=False)
 
 
-@pytest.mark.parametrize("fmt", PLAIN)
+@pytest.mark.parametrize("fmt", ALL)
 def test_all_zero_inputs_reproducer_property(fmt):
     """Zero Q/K/W, windows [0, N-S+row): -inf exactly off-window, 0 in-window."""
     m, n = 64, 1100
@@ -109,7 +112,7 @@ def test_all_zero_inputs_reproducer_property(fmt):
     assert np.all(out[valid] == 0.0)
 
 
-@pytest.mark.parametrize("fmt", PLAIN)
+@pytest.mark.parametrize("fmt", ALL)
 def test_bitwise_deterministic(fmt):
     case = synth.make_case(fmt, 2, 64, 2000, seed=9, windows="causal")
     t = binding.case_to_device(case)
@@ -130,6 +133,17 @@ def test_consecutive_calls_different_shapes_same_stream():
     for c, t in zip(cases, tens):
         ref, den = oracle_rows(c)
         compare(t["out"].cpu().numpy().reshape(-1, c.N), ref, den)
+
+
+@pytest.mark.parametrize("fmt", [synth.FMT_MXFP8, synth.FMT_MXFP4])
+def test_mx_block_scales_are_applied(fmt):
+    """Scale bytes spread over +-8 binades and differing per block, key and
+    head: a wrong scale-factor layout or byte selection breaks parity."""
+    case = synth.make_case(fmt, 1, 8, 600, seed=30 + fmt, windows="full")
+    rng = np.random.default_rng(31)
+    case.q_sf = (case.q_sf.astype(np.int32) + rng.integers(-8, 9, case.q_sf.shape)).astype(np.uint8)
+    case.k_sf = (case.k_sf.astype(np.int32) + rng.integers(-8, 9, case.k_sf.shape)).astype(np.uint8)
+    check_full(case)
 
 
 def test_bf16_w_equals_f32_w_of_same_values():
@@ -158,7 +172,9 @@ def sample_rows(B, S, step):
 
 
 @pytest.mark.parametrize("name,step", [("bf16_batched_causal_4096", 256),
-                                       ("fp8_per_token_2048x32768", 256)])
+                                       ("fp8_per_token_2048x32768", 256),
+                                       ("mxfp8_8192x65536", 512),
+                                       ("mxfp4_irregular_8192x65536", 512)])
 def test_full_size_workload(name, step):
     case = synth.make_workload(name)
     t = binding.case_to_device(case)
@@ -176,5 +192,8 @@ def test_full_size_workload(name, step):
         assert torch.equal(torch.isneginf(out[sl]), outside), f"mask rows {r0}+"
         assert torch.isfinite(out[sl][~outside]).all()
     rows = sample_rows(case.B, case.S, step)
+    if name.startswith("mxfp4"):
+        # the forced-empty rows and their neighbours
+        rows = np.union1d(rows, np.array([r for r in synth.FORCED_EMPTY_ROWS if r < case.S]))
     ref, den = oracle_rows(case, rows=rows)
     compare(out[torch.from_numpy(rows).cuda()].cpu().numpy(), ref, den)
