@@ -69,7 +69,8 @@ typedef enum idx_status {
   IDX_ERR_DEVICE = 6,      /* current device is not compute capability 10.3 (sm_103) */
   IDX_ERR_CUDA = 7,        /* a CUDA runtime call failed (launch, allocation, ...)   */
   IDX_ERR_TIMEOUT = 8,     /* device-side wait gave up; the call's output is invalid */
-  IDX_ERR_UNSUPPORTED = 9  /* valid request this build does not implement            */
+  IDX_ERR_UNSUPPORTED = 9, /* valid request this build does not implement            */
+  IDX_ERR_SCRATCH = 10     /* indexer_logits_noalloc: more scratch than its array   */
 } idx_status;
 
 /* Problem shape and layout. Zero strides mean "dense". */
@@ -128,6 +129,31 @@ IDX_API int indexer_logits(const void* q, const uint8_t* q_sf, const void* k, co
                    const float* k_scales, const void* w, const int32_t* ks, const int32_t* ke,
                    float sm_scale, int clean, float* out, const idx_shape* shape,
                    idx_stream_t stream);
+
+/* Same computation, arguments and checks as indexer_logits, but this call
+ * never allocates device memory, not even on its first use. The pages have no
+ * counterpart; it is here for callers that may not call cudaMalloc: code
+ * running while a stream is being captured into a CUDA graph, allocators and
+ * memory-pool owners, and embedders whose memory budget is fixed up front.
+ *
+ * Its scratch (a work counter, a finished-block count and an error word: 3 of
+ * 64 words) lives in one fixed 256-byte device array inside the library, which
+ * every GPU that loads the library keeps until the process exits. One call
+ * needs the same 3 words whatever its shape, so no shape is turned away for
+ * lack of scratch; IDX_ERR_SCRATCH is returned if a call would need more than
+ * the array holds. The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress, no allocation); make that first call before
+ * any stream capture. Each call clears the three words on `stream` before its
+ * kernel, because the array keeps the previous call's contents. All calls on
+ * a device share the one array, so calls that can overlap on the GPU (on
+ * different streams without ordering) race and must not be issued that way.
+ * A device-side wait that runs out is recorded only in that shared array;
+ * indexer_get_last_error does not report it for this entry point. */
+IDX_API int indexer_logits_noalloc(const void* q, const uint8_t* q_sf, const void* k,
+                                   const uint8_t* k_sf, const float* k_scales, const void* w,
+                                   const int32_t* ks, const int32_t* ke, float sm_scale,
+                                   int clean, float* out, const idx_shape* shape,
+                                   idx_stream_t stream);
 
 /* Human-readable text for an idx_status value (static storage, never NULL). */
 IDX_API const char* indexer_status_string(int status);

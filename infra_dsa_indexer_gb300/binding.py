@@ -59,6 +59,8 @@ def load():
         lib.indexer_logits.restype = i32
         lib.indexer_logits.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, i32,
                                        vp, ctypes.POINTER(idx_shape), vp]
+        lib.indexer_logits_noalloc.restype = i32
+        lib.indexer_logits_noalloc.argtypes = lib.indexer_logits.argtypes
         lib.indexer_status_string.restype = ctypes.c_char_p
         lib.indexer_status_string.argtypes = [i32]
         lib.indexer_get_last_error.restype = i32
@@ -108,6 +110,20 @@ def indexer_logits(q, q_sf, k, k_sf, k_scales, w, ks, ke, sm_scale, clean, out,
                             _ptr(out), ctypes.byref(shape), _stream(stream))
     if st != IDX_OK:
         raise IndexerError(st, "indexer_logits")
+
+
+def indexer_logits_noalloc(q, q_sf, k, k_sf, k_scales, w, ks, ke, sm_scale, clean, out,
+                           shape: idx_shape, stream=None) -> None:
+    """indexer_logits for callers that may not allocate device memory: the
+    library keeps its scratch in one fixed device array instead (see the
+    declaration in include/dsa_indexer.h for the sharing rules)."""
+    lib = load()
+    st = lib.indexer_logits_noalloc(_ptr(q), _ptr(q_sf), _ptr(k), _ptr(k_sf), _ptr(k_scales),
+                                    _ptr(w), _ptr(ks), _ptr(ke), ctypes.c_float(sm_scale),
+                                    int(bool(clean)), _ptr(out), ctypes.byref(shape),
+                                    _stream(stream))
+    if st != IDX_OK:
+        raise IndexerError(st, "indexer_logits_noalloc")
 
 
 def indexer_status_string(status: int) -> str:

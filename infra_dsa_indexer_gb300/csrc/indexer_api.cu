@@ -79,6 +79,32 @@ int get_scratch(int dev, cudaStream_t stream, int32_t** out) {
   return IDX_OK;
 }
 
+// Words of scratch one call uses: [0] unit counter, [1] finished CTAs,
+// [2] device error word.
+constexpr int kScratchWordsPerCall = 3;
+
+// Scratch of indexer_logits_noalloc: a fixed array in the library's device
+// image (every GPU that loads the library holds these 256 bytes until the
+// process exits). Host code may not use its name as a pointer: its device
+// address is looked up once per device with cudaGetSymbolAddress.
+constexpr int kFixedScratchWords = 64;
+constexpr int kMaxDevices = 64;
+__device__ __align__(256) int32_t g_fixed_scratch[kFixedScratchWords];
+int32_t* g_fixed_scratch_addr[kMaxDevices] = {};
+
+// Called with g_mutex held and `dev` current.
+int get_fixed_scratch(int dev, int32_t** out) {
+  if (dev < 0 || dev >= kMaxDevices) return IDX_ERR_DEVICE;
+  if (g_fixed_scratch_addr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_fixed_scratch) != cudaSuccess || ptr == nullptr)
+      return IDX_ERR_CUDA;
+    g_fixed_scratch_addr[dev] = static_cast<int32_t*>(ptr);
+  }
+  *out = g_fixed_scratch_addr[dev];
+  return IDX_OK;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // 2-D or 3-D tiled map. dims/strides in elements/bytes.
@@ -127,6 +153,7 @@ const char* indexer_status_string(int status) {
     case IDX_ERR_CUDA: return "a CUDA runtime call failed";
     case IDX_ERR_TIMEOUT: return "a device-side wait ran out; the output of that call is invalid";
     case IDX_ERR_UNSUPPORTED: return "request not supported by this build";
+    case IDX_ERR_SCRATCH: return "call needs more scratch than the fixed no-allocation array holds";
     default: return "unknown status";
   }
 }
@@ -138,11 +165,17 @@ int64_t indexer_set_wait_limit_ns(int64_t ns) {
   return prev;
 }
 
-int indexer_logits(const void* q, const uint8_t* q_sf, const void* k, const uint8_t* k_sf,
+}  // extern "C"
+
+namespace {
+
+// Validate, build the tensor maps and launch one call. `fixed_scratch` is
+// null for indexer_logits (scratch per (device, stream), allocated on first
+// use) or selects the no-allocation variant's fixed device array.
+int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint8_t* k_sf,
                    const float* k_scales, const void* w, const int32_t* ks, const int32_t* ke,
                    float sm_scale, int clean, float* out, const idx_shape* shape,
-                   idx_stream_t stream_) {
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+                   cudaStream_t stream, bool fixed_scratch) {
   if (!shape || !q || !k || !w || !ks || !ke || !out) return IDX_ERR_NULL;
   const idx_shape sh = *shape;
   if (sh.fmt < IDX_FMT_BF16 || sh.fmt > IDX_FMT_MXFP4) return IDX_ERR_FORMAT;
@@ -182,7 +215,14 @@ int indexer_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
   if (di->cc_major != 10 || di->cc_minor != 3) return IDX_ERR_DEVICE;
   if ((st = get_encoder())) return st;
   int32_t* scratch = nullptr;
-  if ((st = get_scratch(dev, stream, &scratch))) return st;
+  if (fixed_scratch) {
+    if ((st = get_fixed_scratch(dev, &scratch))) return st;
+    // The array keeps the previous call's words: start this one from zero.
+    if (cudaMemsetAsync(scratch, 0, kScratchWordsPerCall * sizeof(int32_t), stream) != cudaSuccess)
+      return IDX_ERR_CUDA;
+  } else if ((st = get_scratch(dev, stream, &scratch))) {
+    return st;
+  }
 
   KernelParams prm;
   std::memset(&prm, 0, sizeof(prm));
@@ -247,6 +287,29 @@ int indexer_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
                             : launch<dsa::kFmtMXFP4, false>(prm, grid, di, stream);
     default: return IDX_ERR_UNSUPPORTED;
   }
+}
+
+}  // namespace
+
+extern "C" {
+
+int indexer_logits(const void* q, const uint8_t* q_sf, const void* k, const uint8_t* k_sf,
+                   const float* k_scales, const void* w, const int32_t* ks, const int32_t* ke,
+                   float sm_scale, int clean, float* out, const idx_shape* shape,
+                   idx_stream_t stream) {
+  return enqueue_logits(q, q_sf, k, k_sf, k_scales, w, ks, ke, sm_scale, clean, out, shape,
+                        reinterpret_cast<cudaStream_t>(stream), false);
+}
+
+int indexer_logits_noalloc(const void* q, const uint8_t* q_sf, const void* k,
+                           const uint8_t* k_sf, const float* k_scales, const void* w,
+                           const int32_t* ks, const int32_t* ke, float sm_scale, int clean,
+                           float* out, const idx_shape* shape, idx_stream_t stream) {
+  // One call needs kScratchWordsPerCall words whatever the shape; refuse
+  // anything that would need more than the fixed array holds.
+  if (kScratchWordsPerCall > kFixedScratchWords) return IDX_ERR_SCRATCH;
+  return enqueue_logits(q, q_sf, k, k_sf, k_scales, w, ks, ke, sm_scale, clean, out, shape,
+                        reinterpret_cast<cudaStream_t>(stream), true);
 }
 
 int indexer_get_last_error(idx_stream_t stream_) {

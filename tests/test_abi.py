@@ -42,7 +42,7 @@ def test_binding_exposes_same_names():
 
 
 def test_status_strings(lib):
-    for st in range(0, 10):
+    for st in range(0, 11):
         assert binding.indexer_status_string(st)
     assert "unknown" in binding.indexer_status_string(12345)
     assert binding.indexer_version() >= 100
@@ -89,6 +89,16 @@ def shp(**kw):
 ])
 def test_host_validation(lib, over, shape_kw, status):
     assert call(lib, shp(**shape_kw), **over) == status
+
+
+@pytest.mark.parametrize("shape_kw,status", [(dict(H=32), 2), (dict(fmt=9), 3),
+                                              (dict(out_row_stride=7), 2)])
+def test_noalloc_entry_validates_like_indexer_logits(lib, shape_kw, status):
+    args = (FAKE, None, FAKE, None, None, FAKE, FAKE, FAKE, ctypes.c_float(0.1), 1, FAKE)
+    assert lib.indexer_logits_noalloc(*args, ctypes.byref(shp(**shape_kw)), None) == status
+    assert lib.indexer_logits_noalloc(FAKE, None, None, None, None, FAKE, FAKE, FAKE,
+                                      ctypes.c_float(0.1), 1, FAKE,
+                                      ctypes.byref(shp()), None) == 1
 
 
 def test_null_shape(lib):
