@@ -266,6 +266,7 @@ def workload_config(case, args):
             "H": case.H, "D": case.D, "format": synth.FMT_NAMES[case.fmt],
             "w_format": "bf16" if case.w_fmt == synth.W_BF16 else "f32",
             "in_window_pairs": case.in_window_pairs(), "clean": bool(case.clean),
+            "group_rows": bool(case.group_rows),
             "l2": "flushed before every timed call (256 MiB write)",
             "parallelism": f"replicas x{args.gpus}"}
 
@@ -286,7 +287,7 @@ def run_ours(args, dist):
     t = binding.case_to_device(case, device=f"cuda:{dev}")
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=f"cuda:{dev}")
-    launches_per_call = binding.indexer_launches_per_call()
+    launches_per_call = binding.indexer_launches_per_call(t["shape"])
 
     for _ in range(args.warmup):
         binding.run_case(case, t, stream=stream)

@@ -73,6 +73,15 @@ typedef enum idx_status {
   IDX_ERR_SCRATCH = 10     /* indexer_logits_noalloc: more scratch than its array   */
 } idx_status;
 
+/* idx_shape.flags: the rows' windows are irregular (not a causal staircase);
+ * group rows with similar windows into the kernel's 4-row blocks. A block
+ * computes the union of its rows' 128-key tiles, so on windows with unrelated
+ * starts and lengths consecutive rows waste about 2.4x the work; grouped, about
+ * 1.03x. Costs one extra launch (a per-batch sort of the rows by window) and
+ * B*S*4 bytes of library scratch on the stream; ignored when S > 16384 and by
+ * indexer_logits_noalloc. The logits do not depend on it. */
+#define IDX_FLAG_GROUP_ROWS 1
+
 /* Problem shape and layout. Zero strides mean "dense". */
 typedef struct idx_shape {
   int32_t B;              /* batches (uniform length), >= 1                          */
@@ -82,7 +91,7 @@ typedef struct idx_shape {
   int32_t D;              /* head dimension, must be 128                               */
   int32_t fmt;            /* idx_format                                                */
   int32_t w_fmt;          /* idx_w_format                                              */
-  int32_t reserved;       /* must be 0                                                 */
+  int32_t flags;          /* IDX_FLAG_* bits, other bits 0                             */
   int64_t q_row_bytes;    /* bytes between consecutive (b,i,h) rows of q; 0 = dense    */
   int64_t k_row_bytes;    /* bytes between consecutive keys of k; 0 = dense            */
   int64_t k_batch_bytes;  /* bytes between batches of k; 0 = N * k_row_bytes           */
@@ -120,10 +129,12 @@ typedef struct idx_shape {
  * Returns IDX_OK once the work is enqueued. Argument errors are detected on
  * the host before any launch. A device-side wait that runs out is reported
  * by indexer_get_last_error(), not here. The first call on a (device,
- * stream) pair allocates a small library-owned scratch block (a few hundred
- * bytes: a work counter and an error word), so make one call before
- * capturing a CUDA graph on that stream; calls on one stream reuse it, so
- * calls on the same stream must not overlap (stream order guarantees that).
+ * stream) pair allocates a small library-owned scratch block (a work counter
+ * and an error word, plus B*S words for IDX_FLAG_GROUP_ROWS; a later call that
+ * needs more frees and re-allocates it, waiting for the device), so make one
+ * call of the largest shape before capturing a CUDA graph on that stream;
+ * calls on one stream reuse it, so calls on the same stream must not overlap
+ * (stream order guarantees that).
  */
 IDX_API int indexer_logits(const void* q, const uint8_t* q_sf, const void* k, const uint8_t* k_sf,
                    const float* k_scales, const void* w, const int32_t* ks, const int32_t* ke,
@@ -169,9 +180,10 @@ IDX_API int indexer_get_last_error(idx_stream_t stream);
  * below 1e6 are raised to 1e6. Returns the previous value. */
 IDX_API int64_t indexer_set_wait_limit_ns(int64_t ns);
 
-/* Number of kernel launches one indexer_logits call makes (for launch counts
- * in benchmarks). */
-IDX_API int indexer_launches_per_call(void);
+/* Number of kernel launches one indexer_logits call with this shape makes
+ * (2 with IDX_FLAG_GROUP_ROWS in effect, else 1); for launch counts in
+ * benchmarks. */
+IDX_API int indexer_launches_per_call(const idx_shape* shape);
 
 /* Free every library-owned scratch block on every device (synchronises each
  * device that has one). Later calls allocate again. Returns IDX_OK or

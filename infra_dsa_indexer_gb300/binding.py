@@ -17,6 +17,7 @@ import torch
 
 IDX_FMT_BF16, IDX_FMT_E4M3, IDX_FMT_MXFP8, IDX_FMT_MXFP4 = 0, 1, 2, 3
 IDX_W_F32, IDX_W_BF16 = 0, 1
+IDX_FLAG_GROUP_ROWS = 1
 IDX_OK = 0
 IDX_ERR_TIMEOUT = 8
 
@@ -35,7 +36,7 @@ class IndexerError(RuntimeError):
 class idx_shape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("S", ctypes.c_int32), ("N", ctypes.c_int32),
                 ("H", ctypes.c_int32), ("D", ctypes.c_int32), ("fmt", ctypes.c_int32),
-                ("w_fmt", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("w_fmt", ctypes.c_int32), ("flags", ctypes.c_int32),
                 ("q_row_bytes", ctypes.c_int64), ("k_row_bytes", ctypes.c_int64),
                 ("k_batch_bytes", ctypes.c_int64), ("out_row_stride", ctypes.c_int64)]
 
@@ -68,7 +69,7 @@ def load():
         lib.indexer_set_wait_limit_ns.restype = i64
         lib.indexer_set_wait_limit_ns.argtypes = [i64]
         lib.indexer_launches_per_call.restype = i32
-        lib.indexer_launches_per_call.argtypes = []
+        lib.indexer_launches_per_call.argtypes = [ctypes.POINTER(idx_shape)]
         lib.indexer_shutdown.restype = i32
         lib.indexer_shutdown.argtypes = []
         lib.indexer_version.restype = i32
@@ -94,8 +95,8 @@ def _stream(stream):
 
 
 def make_shape(B, S, N, H, D, fmt, w_fmt, *, q_row_bytes=0, k_row_bytes=0,
-               k_batch_bytes=0, out_row_stride=0) -> idx_shape:
-    return idx_shape(B, S, N, H, D, fmt, w_fmt, 0, q_row_bytes, k_row_bytes,
+               k_batch_bytes=0, out_row_stride=0, flags=0) -> idx_shape:
+    return idx_shape(B, S, N, H, D, fmt, w_fmt, flags, q_row_bytes, k_row_bytes,
                      k_batch_bytes, out_row_stride)
 
 
@@ -138,8 +139,8 @@ def indexer_set_wait_limit_ns(ns: int) -> int:
     return load().indexer_set_wait_limit_ns(int(ns))
 
 
-def indexer_launches_per_call() -> int:
-    return load().indexer_launches_per_call()
+def indexer_launches_per_call(shape: idx_shape) -> int:
+    return load().indexer_launches_per_call(ctypes.byref(shape))
 
 
 def indexer_shutdown() -> int:
@@ -167,7 +168,8 @@ def case_to_device(case, device="cuda", out_row_stride=None):
     stride = out_row_stride or case.N
     t["out"] = torch.empty((case.B, case.S, stride), dtype=torch.float32, device=device)
     t["shape"] = make_shape(case.B, case.S, case.N, case.H, case.D, case.fmt, case.w_fmt,
-                            out_row_stride=stride)
+                            out_row_stride=stride,
+                            flags=IDX_FLAG_GROUP_ROWS if case.group_rows else 0)
     return t
 
 

@@ -14,6 +14,7 @@
 
 #include "dsa_indexer.h"
 #include "indexer_kernel.cuh"
+#include "plan_kernel.cuh"
 
 namespace {
 
@@ -26,11 +27,19 @@ struct DeviceInfo {
   int sm_count = 0;
   int cc_major = 0, cc_minor = 0;
   bool smem_set[8] = {false, false, false, false, false, false, false, false};
+  bool plan_attr_set = false;
 };
 
 std::mutex g_mutex;
 std::map<int, DeviceInfo> g_devices;
-std::map<std::pair<int, uintptr_t>, int32_t*> g_scratch;
+// Scratch of indexer_logits per (device, stream): kScratchInts header words
+// ([0] unit counter, [1] finished CTAs, [2] error word), then the row order
+// of a grouped call (B*S words).
+struct Scratch {
+  int32_t* ptr = nullptr;
+  int64_t words = 0;
+};
+std::map<std::pair<int, uintptr_t>, Scratch> g_scratch;
 int64_t g_wait_limit_ns = 2000000000LL;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -61,22 +70,55 @@ int get_encoder() {
   return IDX_OK;
 }
 
-int get_scratch(int dev, cudaStream_t stream, int32_t** out) {
-  auto key = std::make_pair(dev, reinterpret_cast<uintptr_t>(stream));
-  auto it = g_scratch.find(key);
-  if (it != g_scratch.end()) {
-    *out = it->second;
+// At least `words` words of scratch for (dev, stream). Growing frees the old
+// block (cudaFree waits for the device) and carries the error word over.
+int get_scratch(int dev, cudaStream_t stream, int64_t words, int32_t** out) {
+  words = std::max<int64_t>(words, kScratchInts);
+  Scratch& sc = g_scratch[std::make_pair(dev, reinterpret_cast<uintptr_t>(stream))];
+  if (sc.ptr != nullptr && sc.words >= words) {
+    *out = sc.ptr;
     return IDX_OK;
   }
+  int32_t err = 0;
+  if (sc.ptr != nullptr) {
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(&err, sc.ptr + 2, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaFree(sc.ptr) != cudaSuccess)
+      return IDX_ERR_CUDA;
+    sc.ptr = nullptr;
+    sc.words = 0;
+  }
   int32_t* p = nullptr;
-  if (cudaMalloc(&p, kScratchInts * sizeof(int32_t)) != cudaSuccess) return IDX_ERR_CUDA;
-  if (cudaMemset(p, 0, kScratchInts * sizeof(int32_t)) != cudaSuccess) {
+  if (cudaMalloc(&p, words * sizeof(int32_t)) != cudaSuccess) return IDX_ERR_CUDA;
+  if (cudaMemset(p, 0, kScratchInts * sizeof(int32_t)) != cudaSuccess ||
+      (err != 0 && cudaMemcpy(p + 2, &err, sizeof(err), cudaMemcpyHostToDevice) != cudaSuccess)) {
     cudaFree(p);
     return IDX_ERR_CUDA;
   }
-  g_scratch[key] = p;
+  sc.ptr = p;
+  sc.words = words;
   *out = p;
   return IDX_OK;
+}
+
+// Rows are regrouped by window (one planning launch before the logits
+// kernel) when the caller asks for it, the call may allocate, and one batch's
+// rows fit the planner's shared memory.
+bool groups_rows(const idx_shape& sh, bool fixed_scratch) {
+  return (sh.flags & IDX_FLAG_GROUP_ROWS) != 0 && !fixed_scratch && sh.S <= dsa::kPlanMaxRows;
+}
+
+int launch_plan(const int32_t* ks, const int32_t* ke, const idx_shape& sh, int32_t* perm,
+                DeviceInfo* di, cudaStream_t stream) {
+  const int smem = dsa::plan_pow2(sh.S) * static_cast<int>(sizeof(uint64_t));
+  if (!di->plan_attr_set) {
+    if (cudaFuncSetAttribute(dsa::plan_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dsa::kPlanMaxRows * static_cast<int>(sizeof(uint64_t))) != cudaSuccess)
+      return IDX_ERR_CUDA;
+    di->plan_attr_set = true;
+  }
+  dsa::plan_rows_kernel<<<sh.B, dsa::kPlanThreads, smem, stream>>>(ks, ke, sh.S, sh.N, perm);
+  return cudaGetLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }
 
 // Words of scratch one call uses: [0] unit counter, [1] finished CTAs,
@@ -139,7 +181,9 @@ extern "C" {
 
 int indexer_version(void) { return 100; }
 
-int indexer_launches_per_call(void) { return 1; }
+int indexer_launches_per_call(const idx_shape* shape) {
+  return shape != nullptr && groups_rows(*shape, false) ? 2 : 1;
+}
 
 const char* indexer_status_string(int status) {
   switch (status) {
@@ -184,7 +228,8 @@ int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
   if (mx && (!q_sf || !k_sf)) return IDX_ERR_NULL;
   if (!mx && (q_sf || k_sf)) return IDX_ERR_FORMAT;
   if (k_scales && sh.fmt != IDX_FMT_E4M3) return IDX_ERR_FORMAT;
-  if (sh.H != dsa::kHeads || sh.D != dsa::kHeadDim || sh.reserved != 0) return IDX_ERR_SHAPE;
+  if (sh.H != dsa::kHeads || sh.D != dsa::kHeadDim || (sh.flags & ~IDX_FLAG_GROUP_ROWS) != 0)
+    return IDX_ERR_SHAPE;
   if (sh.B < 1 || sh.S < 1 || sh.S % dsa::kRowsPerBlock != 0 || sh.N < 1) return IDX_ERR_SHAPE;
   if (!std::isfinite(sm_scale)) return IDX_ERR_SCALE;
 
@@ -220,7 +265,9 @@ int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
     // The array keeps the previous call's words: start this one from zero.
     if (cudaMemsetAsync(scratch, 0, kScratchWordsPerCall * sizeof(int32_t), stream) != cudaSuccess)
       return IDX_ERR_CUDA;
-  } else if ((st = get_scratch(dev, stream, &scratch))) {
+  } else if ((st = get_scratch(dev, stream,
+                                kScratchInts + (groups_rows(sh, fixed_scratch) ? total_rows : 0),
+                                &scratch))) {
     return st;
   }
 
@@ -236,7 +283,7 @@ int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
   {
     const uint64_t dims[2] = {row_elems, static_cast<uint64_t>(total_rows * sh.H)};
     const uint64_t strides[1] = {static_cast<uint64_t>(q_row)};
-    const uint32_t box[2] = {panel_elems, static_cast<uint32_t>(dsa::kBlockN)};
+    const uint32_t box[2] = {panel_elems, static_cast<uint32_t>(dsa::kHeads)};  // one row
     if ((st = encode_map(&prm.tmap_q, q, dt, 2, dims, strides, box, swz))) return st;
   }
   {
@@ -277,6 +324,10 @@ int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
   prm.nchunk = static_cast<int32_t>(nchunk);
   prm.num_units = static_cast<int32_t>(units);
   const int grid = static_cast<int>(std::min<int64_t>(di->sm_count, units));
+  if (groups_rows(sh, fixed_scratch)) {
+    prm.perm = scratch + kScratchInts;
+    if ((st = launch_plan(ks, ke, sh, const_cast<int32_t*>(prm.perm), di, stream))) return st;
+  }
 
   switch (sh.fmt) {
     case IDX_FMT_BF16: return launch<dsa::kFmtBF16, false>(prm, grid, di, stream);
@@ -320,8 +371,8 @@ int indexer_get_last_error(idx_stream_t stream_) {
   {
     std::lock_guard<std::mutex> lock(g_mutex);
     auto it = g_scratch.find(std::make_pair(dev, reinterpret_cast<uintptr_t>(stream)));
-    if (it == g_scratch.end()) return IDX_OK;
-    scratch = it->second;
+    if (it == g_scratch.end() || it->second.ptr == nullptr) return IDX_OK;
+    scratch = it->second.ptr;
   }
   if (cudaStreamSynchronize(stream) != cudaSuccess) return IDX_ERR_CUDA;
   int32_t word = 0;
@@ -342,8 +393,9 @@ int indexer_shutdown(void) {
   int cur = 0;
   cudaGetDevice(&cur);
   for (auto& kv : g_scratch) {
+    if (kv.second.ptr == nullptr) continue;
     if (cudaSetDevice(kv.first.first) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess ||
-        cudaFree(kv.second) != cudaSuccess)
+        cudaFree(kv.second.ptr) != cudaSuccess)
       rc = IDX_ERR_CUDA;
   }
   g_scratch.clear();

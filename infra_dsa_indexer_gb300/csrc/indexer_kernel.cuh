@@ -75,7 +75,7 @@ enum : int { kErrTimeout = 8, kErrAlign = 4 };
 struct UnitInfo {
   int32_t stop;
   int32_t b;
-  int32_t grow0;     // flattened row id b*S + i of the block's first row
+  int32_t row[4];    // flattened row ids b*S + i of the block's rows
   int32_t c0, c1;    // key tiles [c0, c1) computed by this unit
   int32_t t0, t1;    // key tiles [t0, t1) covered by the whole row-block
   int32_t flags;     // bit 0: fill [0, t0*128) with -inf; bit 1: fill [t1*128, N)
@@ -92,6 +92,7 @@ struct KernelParams {
   const void* w;
   const int32_t* ks;
   const int32_t* ke;
+  const int32_t* perm;  // [B,S] row order within each batch, or null (identity)
   float* out;
   int32_t* scratch;  // [0] unit counter, [1] finished CTAs, [2] error word
   int64_t out_row_stride;
@@ -378,12 +379,19 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       const int chunk = u - order * p.nchunk;
       const int blk = p.blocks_per_batch - 1 - order / p.B;
       const int b = order % p.B;
-      const int grow0 = b * p.S + blk * kRowsPerBlock;
-      // head weights of the 4 rows -> FP32 in shared memory
+      // The block's rows: positions 4*blk .. 4*blk+3 of the batch's row order.
+      int grow[kRowsPerBlock];
+#pragma unroll
+      for (int r = 0; r < kRowsPerBlock; ++r) {
+        const int pos = blk * kRowsPerBlock + r;
+        grow[r] = b * p.S + (p.perm != nullptr ? __ldg(p.perm + b * p.S + pos) : pos);
+      }
+      // head weights of the 4 rows -> FP32 in shared memory, row-major 4 x 64
       float* wdst = reinterpret_cast<float*>(wbuf + slot * L::kWBytes);
       if (p.w_bf16) {
+        // lane l: 8 weights = 16 bytes, row l/8, heads 8*(l%8)..
         const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.w) +
-                                static_cast<int64_t>(grow0) * (kHeads / 8) + lane);
+                                static_cast<int64_t>(grow[lane >> 3]) * (kHeads / 8) + (lane & 7));
         const uint32_t r[4] = {raw.x, raw.y, raw.z, raw.w};
         reinterpret_cast<float4*>(wdst)[2 * lane] =
             make_float4(__uint_as_float(r[0] << 16), __uint_as_float(r[0] & 0xffff0000u),
@@ -392,21 +400,25 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
             make_float4(__uint_as_float(r[2] << 16), __uint_as_float(r[2] & 0xffff0000u),
                         __uint_as_float(r[3] << 16), __uint_as_float(r[3] & 0xffff0000u));
       } else {
-        const float4* src = reinterpret_cast<const float4*>(p.w) +
-                            static_cast<int64_t>(grow0) * (kHeads / 4);
-        reinterpret_cast<float4*>(wdst)[lane] = __ldg(src + lane);
-        reinterpret_cast<float4*>(wdst)[lane + 32] = __ldg(src + lane + 32);
+        // float4 f (lane and lane + 32): row f/16, heads 4*(f%16)..
+        const float4* src = reinterpret_cast<const float4*>(p.w);
+#pragma unroll
+        for (int f = lane; f < kRowsPerBlock * kHeads / 4; f += 32)
+          reinterpret_cast<float4*>(wdst)[f] =
+              __ldg(src + static_cast<int64_t>(grow[f >> 4]) * (kHeads / 4) + (f & 15));
       }
       if constexpr (T::kMX) {
         // Q scale word of (row, head) m = 32c + lane goes to TMEM lane m % 32,
         // column m / 32: in shared memory, chunk m / 128 (one TMEM copy
         // each), row m % 32 (16 bytes), word (m % 128) / 32.
-        const uint8_t* src = p.q_sf + static_cast<int64_t>(grow0) * kHeads * 4;
+        // (row, head) m = 64r + h reads the word of row grow[r], head h.
         uint8_t* dst = sfb_s + slot * kSfbBytes;
 #pragma unroll
         for (int c = 0; c < kBlockN / 32; ++c) {
           const int m = 32 * c + lane;
-          cp_async_4(dst + (m >> 7) * 512 + 16 * lane + 4 * (c & 3), src + 4 * m);
+          const uint8_t* src =
+              p.q_sf + (static_cast<int64_t>(grow[m >> 6]) * kHeads + (m & 63)) * 4;
+          cp_async_4(dst + (m >> 7) * 512 + 16 * lane + 4 * (c & 3), src);
         }
         cp_async_arrive(&unit_full[slot]);
       }
@@ -415,8 +427,9 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         int lo_all = p.N, hi_all = 0;
 #pragma unroll
         for (int r = 0; r < kRowsPerBlock; ++r) {
-          const int lo = clampi(__ldg(p.ks + grow0 + r), 0, p.N);
-          const int hi = clampi(__ldg(p.ke + grow0 + r), 0, p.N);
+          const int lo = clampi(__ldg(p.ks + grow[r]), 0, p.N);
+          const int hi = clampi(__ldg(p.ke + grow[r]), 0, p.N);
+          in.row[r] = grow[r];
           in.lo[r] = lo;
           in.hi[r] = hi;
           if (lo < hi) {
@@ -434,7 +447,6 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         const int c1 = min(t1, c0 + len);
         in.stop = 0;
         in.b = b;
-        in.grow0 = grow0;
         in.c0 = c0;
         in.c1 = c1;
         in.t0 = t0;
@@ -442,11 +454,16 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         in.flags = (chunk == 0 ? 1 : 0) | (chunk == p.nchunk - 1 ? 2 : 0);
         if (c1 > c0) {
           mbar_arrive_expect_tx(&unit_full[slot], L::kQBlockBytes);
+          // One 64-head box per row and panel; row r lands at rows 64r.. of
+          // the block (a whole number of swizzle atoms).
           uint8_t* qdst = qbuf + slot * L::kQBlockBytes;
 #pragma unroll
-          for (int pnl = 0; pnl < L::kPanels; ++pnl)
-            tma_load_2d(qdst + pnl * L::kQPanelBytes, &p.tmap_q, &unit_full[slot],
-                        pnl * (T::kSwizzleBytes / T::kTmaElemBytes), grow0 * kHeads, pol_first);
+          for (int r = 0; r < kRowsPerBlock; ++r)
+#pragma unroll
+            for (int pnl = 0; pnl < L::kPanels; ++pnl)
+              tma_load_2d(qdst + pnl * L::kQPanelBytes + r * kHeads * T::kSwizzleBytes,
+                          &p.tmap_q, &unit_full[slot], pnl * (T::kSwizzleBytes / T::kTmaElemBytes),
+                          grow[r] * kHeads, pol_first);
         } else {
           mbar_arrive(&unit_full[slot]);
         }
@@ -626,7 +643,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       for (int r = 0; r < R; ++r) {
         lo[r] = in.lo[r0 + r];
         hi[r] = in.hi[r0 + r];
-        orow[r] = p.out + static_cast<int64_t>(in.grow0 + r0 + r) * p.out_row_stride;
+        orow[r] = p.out + static_cast<int64_t>(in.row[r0 + r]) * p.out_row_stride;
       }
       const float* wrows = reinterpret_cast<const float*>(wbuf + slot * L::kWBytes) + r0 * kHeads;
       if (p.clean && (flags & 1)) {

@@ -54,6 +54,7 @@ class Case:
     k_sf: np.ndarray | None = None  # [B,N,D/32] uint8 E8M0
     k_tok: np.ndarray | None = None  # [B,N] float32 per-token K scale
     clean: bool = True
+    group_rows: bool = False      # windows are irregular: ask the call to group rows
 
     def in_window_pairs(self) -> int:
         lo = np.clip(self.ks.astype(np.int64), 0, self.N)
@@ -158,7 +159,7 @@ def irregular_windows(rng, B, S, N, forced_empty=FORCED_EMPTY_ROWS):
 
 def make_case(fmt, B, S, N, H=64, D=128, *, seed=0, windows="full",
               w_fmt=W_F32, w_std=1.0 / 8.0, sm_scale=None, ks=None, ke=None,
-              zero=False, name=None, mx_unit_scales=False) -> Case:
+              zero=False, name=None, mx_unit_scales=False, group_rows=False) -> Case:
     """Draw Q, K ~ N(0,1), W ~ N(0, w_std^2), quantise to `fmt`.
 
     windows: "full" ([0,N)), "causal" ([0, N-S+i+1)), "causal_excl"
@@ -219,7 +220,8 @@ def make_case(fmt, B, S, N, H=64, D=128, *, seed=0, windows="full",
     ke = np.ascontiguousarray(np.broadcast_to(np.asarray(ke, dtype=np.int32), (B, S)))
     return Case(name=name or f"{FMT_NAMES[fmt]}_B{B}_S{S}_N{N}", fmt=fmt, B=B,
                 S=S, N=N, H=H, D=D, sm_scale=sm_scale, q=q, k=k, w=w,
-                w_fmt=w_fmt, ks=ks, ke=ke, q_sf=q_sf, k_sf=k_sf, k_tok=k_tok)
+                w_fmt=w_fmt, ks=ks, ke=ke, q_sf=q_sf, k_sf=k_sf, k_tok=k_tok,
+                group_rows=group_rows)
 
 
 # The five workloads, by what they are. Seed = position in this list.
@@ -233,7 +235,8 @@ WORKLOADS = {
     "mxfp8_8192x65536": dict(fmt=FMT_MXFP8, B=1, S=8192, N=65536,
                              windows="causal_excl", w_fmt=W_F32, seed=3),
     "mxfp4_irregular_8192x65536": dict(fmt=FMT_MXFP4, B=1, S=8192, N=65536,
-                                       windows="irregular", w_fmt=W_F32, seed=4),
+                                       windows="irregular", w_fmt=W_F32, seed=4,
+                                       group_rows=True),
 }
 
 

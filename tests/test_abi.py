@@ -46,7 +46,9 @@ def test_status_strings(lib):
         assert binding.indexer_status_string(st)
     assert "unknown" in binding.indexer_status_string(12345)
     assert binding.indexer_version() >= 100
-    assert binding.indexer_launches_per_call() >= 1
+    assert binding.indexer_launches_per_call(shp()) == 1
+    assert binding.indexer_launches_per_call(shp(flags=1)) == 2
+    assert binding.indexer_launches_per_call(shp(flags=1, S=16388)) == 1
 
 
 FAKE = ctypes.c_void_p(0x1000)      # never dereferenced: validation fails first
@@ -63,7 +65,7 @@ def call(lib, shape, **over):
 
 
 def shp(**kw):
-    base = dict(B=1, S=8, N=100, H=64, D=128, fmt=0, w_fmt=0)
+    base = dict(B=1, S=8, N=100, H=64, D=128, fmt=0, w_fmt=0, flags=0)
     base.update(kw)
     return binding.make_shape(**base)
 
@@ -76,6 +78,7 @@ def shp(**kw):
     ({}, dict(S=6), 2),
     ({}, dict(N=0), 2),
     ({}, dict(B=0), 2),
+    ({}, dict(flags=2), 2),                               # unknown flag bit
     ({}, dict(out_row_stride=50), 2),
     ({}, dict(fmt=7), 3),
     ({}, dict(w_fmt=3), 3),

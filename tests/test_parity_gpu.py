@@ -65,6 +65,35 @@ def test_random_windows_ragged(fmt, w_fmt):
     check_full(case)
 
 
+@pytest.mark.parametrize("fmt", ALL)
+def test_grouped_rows_irregular_windows(fmt):
+    """IDX_FLAG_GROUP_ROWS reorders rows into blocks of similar windows: parity
+    with the oracle, and the same bits as the ungrouped call (every element's
+    reduction is unchanged; only which rows share a block differs)."""
+    rng = np.random.default_rng(200 + fmt)
+    B, S, N = 2, 64, 3000
+    ks = rng.integers(0, N // 2, size=(B, S))
+    ke = ks + rng.integers(0, N // 2 + 1, size=(B, S))
+    ke[0, 5] = ks[0, 5]                       # an empty row
+    case = synth.make_case(fmt, B, S, N, seed=60 + fmt, ks=ks, ke=ke)
+    plain = gpu_run(case)
+    case.group_rows = True
+    grouped = check_full(case) is not None and gpu_run(case)
+    assert np.array_equal(plain.view(np.int32), grouped.view(np.int32))
+
+
+def test_grouped_scratch_grows_across_calls():
+    """Grouped calls of growing size on one stream re-size the library's
+    scratch; every result stays right, and so does an ungrouped call after."""
+    for S in (8, 256, 1024):
+        rng = np.random.default_rng(S)
+        ks = rng.integers(0, 400, size=(1, S))
+        ke = ks + rng.integers(0, 401, size=(1, S))
+        case = synth.make_case(synth.FMT_E4M3, 1, S, 800, seed=S, ks=ks, ke=ke, group_rows=True)
+        check_full(case)
+    check_full(synth.make_case(synth.FMT_BF16, 1, 16, 300, seed=3, windows="causal"))
+
+
 @pytest.mark.parametrize("N", [1, 127, 129, 999])
 @pytest.mark.parametrize("fmt", ALL)
 def test_ragged_key_tails(N, fmt):
