@@ -123,6 +123,7 @@ struct Traits<kFmtBF16> {
   static constexpr int kRowsPerWarp = 2;
   static constexpr bool kMX = false;
   static constexpr int kSfIdStep = 0;
+  static constexpr bool kReluAllAdd = true;  // packed-add ReLU on every head pair (RowAcc)
 };
 
 template <>
@@ -136,6 +137,7 @@ struct Traits<kFmtE4M3> {
   static constexpr int kRowsPerWarp = 1;
   static constexpr bool kMX = false;
   static constexpr int kSfIdStep = 0;
+  static constexpr bool kReluAllAdd = false;  // packed-add ReLU on every head pair (RowAcc)
 };
 
 template <>
@@ -151,6 +153,7 @@ struct Traits<kFmtMXFP8> {
   static constexpr int kRowsPerWarp = 1;
   static constexpr bool kMX = true;
   static constexpr int kSfIdStep = 1;
+  static constexpr bool kReluAllAdd = true;  // packed-add ReLU on every head pair (RowAcc)
 };
 
 template <>
@@ -165,6 +168,7 @@ struct Traits<kFmtMXFP4> {
   static constexpr int kRowsPerWarp = 1;
   static constexpr bool kMX = true;
   static constexpr int kSfIdStep = 2;
+  static constexpr bool kReluAllAdd = true;  // packed-add ReLU on every head pair (RowAcc)
 };
 
 template <int FMT>
@@ -212,12 +216,15 @@ __device__ __forceinline__ void fill_neg_inf(float* row, int a, int b, int tid12
 }
 
 // sum_h w[h] * R(x[h]) over the 64 heads of a row, R(x) = max(x, 0) (NEG:
-// min(x, 0)). Heads are taken in groups of four: two through max/min on the
-// ALU pipe, two through x + |x| = 2 max(x, 0) (x - |x| = 2 min(x, 0)) on the
-// FMA pipe, each pair then multiply-accumulated with one packed FP32x2 FMA,
-// so both pipes share the work. The doubled half is scaled by 1/2 at the end
-// (exact). NEG is used only where the MMA cannot negate its A operand.
-template <bool NEG>
+// min(x, 0)), taken four heads at a time and multiply-accumulated pairwise
+// with packed FP32x2 FMAs. The ReLU of a pair is either two max on the ALU
+// pipe, or one packed add x + |x| = 2 max(x, 0) on the FMA pipe (the packed
+// add takes |x| as an operand modifier: one instruction for two heads).
+// ALL_ADD uses the packed add for every pair; otherwise half the pairs use
+// max, which balances the two pipes where the epilogue is the bottleneck.
+// Doubled sums are halved at the end (exact). NEG is used only where the MMA
+// cannot negate its A operand; it takes the scalar min / x - |x| forms.
+template <bool NEG, bool ALL_ADD>
 struct RowAcc {
   float2 m0, m1, d0, d1;
   __device__ __forceinline__ void zero() { m0 = m1 = d0 = d1 = make_float2(0.f, 0.f); }
@@ -227,8 +234,11 @@ struct RowAcc {
       rm = make_float2(fminf(x0, 0.f), fminf(x1, 0.f));
       rd = make_float2(x2 - fabsf(x2), x3 - fabsf(x3));
     } else {
-      rm = make_float2(fmaxf(x0, 0.f), fmaxf(x1, 0.f));
-      rd = make_float2(x2 + fabsf(x2), x3 + fabsf(x3));
+      if constexpr (ALL_ADD)
+        rm = __fadd2_rn(make_float2(x0, x1), make_float2(fabsf(x0), fabsf(x1)));
+      else
+        rm = make_float2(fmaxf(x0, 0.f), fmaxf(x1, 0.f));
+      rd = __fadd2_rn(make_float2(x2, x3), make_float2(fabsf(x2), fabsf(x3)));
     }
     if (g & 1) {
       m1 = __ffma2_rn(make_float2(w.x, w.y), rm, m1);
@@ -241,16 +251,17 @@ struct RowAcc {
   __device__ __forceinline__ float total() const {
     const float sm = (m0.x + m0.y) + (m1.x + m1.y);
     const float sd = (d0.x + d0.y) + (d1.x + d1.y);
+    if constexpr (ALL_ADD && !NEG) return 0.5f * (sm + sd);
     return fmaf(sd, 0.5f, sm);
   }
 };
 
 // R rows at once: v[r] holds row r's 64 accumulator columns, w + r*64 its
 // 64 FP32 weights in shared memory. Rows are interleaved for ILP.
-template <int R, bool NEG>
+template <int R, bool NEG, bool ALL_ADD>
 __device__ __forceinline__ void head_reduce(const uint32_t (&v)[R][64], const float* w,
                                             float (&out)[R]) {
-  RowAcc<NEG> a[R];
+  RowAcc<NEG, ALL_ADD> a[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) a[r].zero();
 #pragma unroll
@@ -549,19 +560,16 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       const int c0 = in.c0, c1 = in.c1;
       const uint64_t b_base = q_desc0 + ((slot * L::kQBlockBytes) >> 4);
       bool ok = true;
-      bool ready = false;  // barriers of tile t already seen complete
       for (int t = c0; t < c1; ++t, ++kiter, ++aiter) {
         const int st = kiter % T::kStages;
         const int acc = aiter % kAccBufs;
         const uint32_t kpar = (kiter / T::kStages) & 1;
-        if (!ready) {
-          if (!mbar_wait(&k_full[st], kpar, abort_flag, p.timeout_ns) ||
-              (T::kMX && !mbar_wait(&sf_full[st], kpar, abort_flag, p.timeout_ns)) ||
-              !mbar_wait(&acc_empty[acc], ((aiter / kAccBufs) & 1) ^ 1, abort_flag,
-                         p.timeout_ns)) {
-            ok = false;
-            break;
-          }
+        if (!mbar_wait(&k_full[st], kpar, abort_flag, p.timeout_ns) ||
+            (T::kMX && !mbar_wait(&sf_full[st], kpar, abort_flag, p.timeout_ns)) ||
+            !mbar_wait(&acc_empty[acc], ((aiter / kAccBufs) & 1) ^ 1, abort_flag,
+                       p.timeout_ns)) {
+          ok = false;
+          break;
         }
         tc_fence_after();
         uint32_t sfa = 0, sfb = 0;
@@ -585,14 +593,6 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         // address >> 4), so every step is the stage/slot base plus an offset.
         const uint64_t a_base = k_desc0 + ((st * L::kKTileBytes) >> 4);
         const uint32_t d_tmem = tmem_base + acc * kBlockN;
-        // The next tile's barriers are polled (non-blocking) between MMA
-        // issues: an issue waits for room in the tensor pipe, so the polls
-        // ride under execution instead of idling the pipe after the tile.
-        const bool has_next = t + 1 < c1;
-        const uint32_t nst = (kiter + 1) % T::kStages, npar = ((kiter + 1) / T::kStages) & 1;
-        const uint32_t nacc = (aiter + 1) % kAccBufs;
-        const uint32_t napar = (((aiter + 1) / kAccBufs) & 1) ^ 1;
-        bool next_k = !has_next, next_s = !has_next || !T::kMX, next_a = !has_next;
 #pragma unroll
         for (int kk = 0; kk < L::kSteps; ++kk) {
           const uint32_t pnl = kk / L::kStepsPerPanel, step = kk % L::kStepsPerPanel;
@@ -602,15 +602,9 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
           const uint32_t id = T::kMX ? (idesc | (sf_id << 4) | (sf_id << 29)) : idesc;
           mma_step<T::kKind>(d_tmem, a_base + (off >> 4), b_base + (offq >> 4), id,
                              kk > 0 ? 1u : 0u, sfa, sfb);
-          if (!next_k) next_k = mbar_test(&k_full[nst], npar);
-          if constexpr (T::kMX) {
-            if (!next_s) next_s = mbar_test(&sf_full[nst], npar);
-          }
-          if (!next_a) next_a = mbar_test(&acc_empty[nacc], napar);
         }
         tc_commit(&k_empty[st]);
         tc_commit(&acc_full[acc]);
-        ready = has_next && next_k && next_s && next_a;
       }
       if (!ok) {
         raise_error(p.scratch, abort_flag, kErrTimeout);
@@ -673,7 +667,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[acc]);
         float sums[R];
-        head_reduce<R, NEG_EPI>(v, wrows, sums);
+        head_reduce<R, NEG_EPI, T::kReluAllAdd>(v, wrows, sums);
         if (j < p.N) {
 #pragma unroll
           for (int r = 0; r < R; ++r)
