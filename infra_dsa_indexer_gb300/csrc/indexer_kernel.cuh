@@ -644,13 +644,21 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
 #pragma unroll
         for (int r = 0; r < R; ++r) fill_neg_inf(orow[r], 0, t0 * kKeysPerTile, tid128);
       }
+      // Per-key scale (E4M3), loaded one tile ahead so that its latency
+      // overlaps the previous tile instead of stalling the loop head.
+      const bool key_scaled = FMT == kFmtE4M3 && p.k_scales != nullptr;
+      const float* kscale_b = key_scaled ? p.k_scales + static_cast<int64_t>(b) * p.N : nullptr;
+      auto load_kscale = [&](int t) {
+        const int jj = t * kKeysPerTile + quarter * 32 + lane;
+        return (key_scaled && t < c1 && jj < p.N) ? __ldg(kscale_b + jj) : 1.f;
+      };
+      float kscale_next = load_kscale(c0);
       bool ok = true;
       for (int t = c0; t < c1; ++t, ++aiter) {
         const int acc = aiter % kAccBufs;
         const int j = t * kKeysPerTile + quarter * 32 + lane;
-        float scale = sm_abs;
-        if (FMT == kFmtE4M3 && p.k_scales != nullptr && j < p.N)
-          scale *= __ldg(p.k_scales + static_cast<int64_t>(b) * p.N + j);
+        const float kscale = kscale_next;
+        kscale_next = load_kscale(t + 1);
         if (!mbar_wait(&acc_full[acc], (aiter / kAccBufs) & 1, abort_flag, p.timeout_ns)) {
           ok = false;
           break;
@@ -671,7 +679,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         if (j < p.N) {
 #pragma unroll
           for (int r = 0; r < R; ++r)
-            __stcs(orow[r] + j, (j >= lo[r] && j < hi[r]) ? sums[r] * scale : ninf);
+            __stcs(orow[r] + j, (j >= lo[r] && j < hi[r]) ? sums[r] * (sm_abs * kscale) : ninf);
         }
       }
       if (!ok) {
