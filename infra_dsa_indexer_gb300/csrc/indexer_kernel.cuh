@@ -564,10 +564,13 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         const int st = kiter % T::kStages;
         const int acc = aiter % kAccBufs;
         const uint32_t kpar = (kiter / T::kStages) & 1;
+        // With a single accumulator its release is on the critical path:
+        // poll for it rather than sleep.
+        const uint32_t apar = ((aiter / kAccBufs) & 1) ^ 1;
         if (!mbar_wait(&k_full[st], kpar, abort_flag, p.timeout_ns) ||
             (T::kMX && !mbar_wait(&sf_full[st], kpar, abort_flag, p.timeout_ns)) ||
-            !mbar_wait(&acc_empty[acc], ((aiter / kAccBufs) & 1) ^ 1, abort_flag,
-                       p.timeout_ns)) {
+            !(kAccBufs > 1 ? mbar_wait(&acc_empty[acc], apar, abort_flag, p.timeout_ns)
+                           : mbar_wait_poll(&acc_empty[acc], apar, abort_flag, p.timeout_ns))) {
           ok = false;
           break;
         }

@@ -49,24 +49,43 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking test of the phase with the given parity.
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+// try_wait with a suspend-time hint: if the phase is still open the thread is
+// suspended until it completes or about `ns` nanoseconds pass.
+__device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, uint32_t parity, uint32_t ns) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
       : "memory");
   return ok != 0;
 }
 
+constexpr uint32_t kSuspendHintNs = 20000;
+
 // Bounded wait for the phase with the given parity to complete. Returns false
-// when `*abort` becomes non-zero or the deadline passes; the clock is read only
-// after the first few thousand polls, so the fast path is a plain try_wait loop.
+// when `*abort` becomes non-zero or the deadline passes. After one immediate
+// test the thread suspends in try_wait (hint above) and is woken when the
+// phase completes, so a waiting warp takes no issue slots from the warps that
+// share its scheduler; abort and deadline are checked between suspensions.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           volatile int* abort, uint64_t timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t start = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait_for(bar, parity, kSuspendHintNs)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - start > timeout_ns) return false;
+  }
+}
+
+// Same contract, polling back to back: for a wait on the critical path, where
+// the wake-up delay of a suspended thread would show. The clock is read only
+// after the first few thousand polls.
+__device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity,
+                                               volatile int* abort, uint64_t timeout_ns) {
   for (int i = 0; i < 4096; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   const uint64_t start = globaltimer_ns();
