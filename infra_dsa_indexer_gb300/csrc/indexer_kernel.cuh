@@ -46,8 +46,8 @@
 //               hides the epilogue's latency better when the MMA is short.
 // Pipelines (mbarriers): unit slots x2 (unit info + Q block + W [+ Q scales]),
 // key-tile ring (kStages) [+ key scales], TMEM accumulators: two 256-column
-// buffers, or one for the MX formats (their scale factors use the rest), so
-// the MMA of tile t+1 overlaps the epilogue of tile t.
+// buffers, so the MMA of tile t+1 overlaps the epilogue of tile t, or one for
+// the MX formats (their scale factors need TMEM too: two slots each).
 #pragma once
 #include <cuda.h>
 #include <cstdint>
@@ -64,8 +64,8 @@ constexpr int kHeadDim = 128;                    // MMA K per tile
 constexpr int kEpiWarp0 = 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kStepBytes = 32;                   // bytes of K per MMA instruction
-constexpr uint32_t kSfaCol = 256;                // MX: key scale factors (4 columns)
-constexpr uint32_t kSfbCol = 260;                // MX: Q scale factors (8 columns)
+constexpr uint32_t kSfaCol = 256;                // MX: key scale factors, 2 slots x 4 columns
+constexpr uint32_t kSfbCol = 264;                // MX: Q scale factors, 2 slots x 8 columns
 constexpr int kSfaBytes = kKeysPerTile * 4;      // one 32-bit word (4 E8M0) per key
 constexpr int kSfbBytes = kBlockN * 4;           // one word per (row, head)
 
@@ -537,7 +537,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // --------------------------------------------------------------- MMA issuer
-    uint32_t kiter = 0, aiter = 0;
+    uint32_t kiter = 0, aiter = 0, units_mma = 0;
     // ReLU(s*x) = |s| * max(-x, 0) for s < 0: negate the A operand (bit 13),
     // except where the epilogue applies the sign (NEG_EPI).
     const uint32_t idesc = T::kIdesc | (!NEG_EPI && p.sm_scale < 0.f ? (1u << 13) : 0u);
@@ -564,27 +564,26 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         const int st = kiter % T::kStages;
         const int acc = aiter % kAccBufs;
         const uint32_t kpar = (kiter / T::kStages) & 1;
-        // With a single accumulator its release is on the critical path:
-        // poll for it rather than sleep.
         const uint32_t apar = ((aiter / kAccBufs) & 1) ^ 1;
         if (!mbar_wait(&k_full[st], kpar, abort_flag, p.timeout_ns) ||
-            (T::kMX && !mbar_wait(&sf_full[st], kpar, abort_flag, p.timeout_ns)) ||
-            !(kAccBufs > 1 ? mbar_wait(&acc_empty[acc], apar, abort_flag, p.timeout_ns)
-                           : mbar_wait_poll(&acc_empty[acc], apar, abort_flag, p.timeout_ns))) {
+            (T::kMX && !mbar_wait(&sf_full[st], kpar, abort_flag, p.timeout_ns))) {
           ok = false;
           break;
         }
         tc_fence_after();
         uint32_t sfa = 0, sfb = 0;
         if constexpr (T::kMX) {
-          // The scale words were written by cp.async (generic proxy); the
-          // TMEM copy reads them through the async proxy. The copies run in
-          // issue order ahead of the MMAs below; one TMEM copy of each kind
-          // is in flight at a time because every tile waits for the
-          // accumulator, i.e. for the previous tile's MMAs to finish.
+          // Scale factors go to TMEM before the accumulator wait, so the copy
+          // is off the critical path: slots alternate (key scales by tile, Q
+          // scales by unit with tiles), and the slot written here was last
+          // read by the MMAs of tile t-2 or earlier, which finished before
+          // tile t-1's accumulator could be handed back and its MMAs issued.
+          // Copies and MMAs of this thread run in issue order. The scale
+          // words were written by cp.async (generic proxy); the TMEM copy
+          // reads them through the async proxy.
           fence_proxy_async_smem();
-          sfa = tmem_base + kSfaCol;
-          sfb = tmem_base + kSfbCol;
+          sfa = tmem_base + kSfaCol + 4 * (kiter & 1);
+          sfb = tmem_base + kSfbCol + 8 * (units_mma & 1);
           if (t == c0) {
             const uint64_t d = sfb_desc0 + ((slot * kSfbBytes) >> 4);
             tc_cp_32x128b_warpx4(sfb, d);
@@ -592,6 +591,14 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
           }
           tc_cp_32x128b_warpx4(sfa, sfa_desc0 + ((st * kSfaBytes) >> 4));
         }
+        // With a single accumulator its release is on the critical path:
+        // poll for it rather than sleep.
+        if (!(kAccBufs > 1 ? mbar_wait(&acc_empty[acc], apar, abort_flag, p.timeout_ns)
+                           : mbar_wait_poll(&acc_empty[acc], apar, abort_flag, p.timeout_ns))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
         // Descriptors differ only in the start-address field (bits 0-13,
         // address >> 4), so every step is the stage/slot base plus an offset.
         const uint64_t a_base = k_desc0 + ((st * L::kKTileBytes) >> 4);
@@ -609,6 +616,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         tc_commit(&k_empty[st]);
         tc_commit(&acc_full[acc]);
       }
+      if (c1 > c0) ++units_mma;
       if (!ok) {
         raise_error(p.scratch, abort_flag, kErrTimeout);
         break;
