@@ -41,9 +41,11 @@
 //               loads its rows' accumulator columns, hands the buffer back to
 //               the MMA warp, then does the ReLU.w head sums, the masked FP32
 //               stores and the -inf fill outside the block's tiles. R = 2
-//               (8 warps, 170 registers each) suits BF16, where the MMA is
-//               long and the role warps need issue slots; R = 1 (16 warps)
-//               hides the epilogue's latency better when the MMA is short.
+//               (8 warps, 168 registers each) halves the per-tile overhead
+//               (waits, stores, loop) and suits BF16, where the MMA is long,
+//               and the MX formats, whose single accumulator serialises MMA
+//               and epilogue anyway; R = 1 (16 warps) hides the epilogue's
+//               latency better for E4M3, whose short MMA is double-buffered.
 // Pipelines (mbarriers): unit slots x2 (unit info + Q block + W [+ Q scales]),
 // key-tile ring (kStages) [+ key scales], TMEM accumulators: two 256-column
 // buffers, so the MMA of tile t+1 overlaps the epilogue of tile t, or one for
@@ -150,7 +152,7 @@ struct Traits<kFmtMXFP8> {
   // scale byte kk of each row's 32-bit scale word.
   static constexpr uint32_t kIdesc = instr_desc_bs(0, 0, kKeysPerTile, kBlockN, 0, 0);
   static constexpr int kKind = 2;
-  static constexpr int kRowsPerWarp = 1;
+  static constexpr int kRowsPerWarp = 2;
   static constexpr bool kMX = true;
   static constexpr int kSfIdStep = 1;
   static constexpr bool kReluAllAdd = true;  // packed-add ReLU on every head pair (RowAcc)
@@ -165,7 +167,7 @@ struct Traits<kFmtMXFP4> {
   // E2M1 x E2M1, UE8M0 scales: MMA step kk (K = 64) uses scale bytes 2kk, 2kk+1.
   static constexpr uint32_t kIdesc = instr_desc_bs(1, 1, kKeysPerTile, kBlockN, 0, 0);
   static constexpr int kKind = 3;
-  static constexpr int kRowsPerWarp = 1;
+  static constexpr int kRowsPerWarp = 2;
   static constexpr bool kMX = true;
   static constexpr int kSfIdStep = 2;
   static constexpr bool kReluAllAdd = true;  // packed-add ReLU on every head pair (RowAcc)
@@ -256,24 +258,20 @@ struct RowAcc {
   }
 };
 
-// R rows at once: v[r] holds row r's 64 accumulator columns, w + r*64 its
-// 64 FP32 weights in shared memory. Rows are interleaved for ILP.
-template <int R, bool NEG, bool ALL_ADD>
-__device__ __forceinline__ void head_reduce(const uint32_t (&v)[R][64], const float* w,
-                                            float (&out)[R]) {
-  RowAcc<NEG, ALL_ADD> a[R];
+// Head groups [G0, G1) (4 heads each) of R rows at once: v[r] holds row r's
+// 64 accumulator columns, w + r*64 its 64 FP32 weights in shared memory.
+// Rows are interleaved for ILP.
+template <int G0, int G1, int R, bool NEG, bool ALL_ADD>
+__device__ __forceinline__ void head_steps(RowAcc<NEG, ALL_ADD> (&a)[R], const uint32_t (&v)[R][64],
+                                           const float* w) {
 #pragma unroll
-  for (int r = 0; r < R; ++r) a[r].zero();
-#pragma unroll
-  for (int g = 0; g < kHeads / 4; ++g) {
+  for (int g = G0; g < G1; ++g) {
 #pragma unroll
     for (int r = 0; r < R; ++r)
       a[r].step(g, reinterpret_cast<const float4*>(w + r * kHeads)[g], __uint_as_float(v[r][4 * g]),
                 __uint_as_float(v[r][4 * g + 1]), __uint_as_float(v[r][4 * g + 2]),
                 __uint_as_float(v[r][4 * g + 3]));
   }
-#pragma unroll
-  for (int r = 0; r < R; ++r) out[r] = a[r].total();
 }
 
 template <int KIND>
@@ -680,13 +678,18 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                acc * kBlockN + r0 * kHeads;
         uint32_t v[R][64];
+        RowAcc<NEG_EPI, T::kReluAllAdd> racc[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) racc[r].zero();
 #pragma unroll
         for (int r = 0; r < R; ++r) tmem_ld_64cols(taddr + r * kHeads, v[r]);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        head_steps<0, kHeads / 4>(racc, v, wrows);
         float sums[R];
-        head_reduce<R, NEG_EPI, T::kReluAllAdd>(v, wrows, sums);
+#pragma unroll
+        for (int r = 0; r < R; ++r) sums[r] = racc[r].total();
         if (j < p.N) {
 #pragma unroll
           for (int r = 0; r < R; ++r)

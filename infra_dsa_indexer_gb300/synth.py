@@ -237,6 +237,14 @@ WORKLOADS = {
     "mxfp4_irregular_8192x65536": dict(fmt=FMT_MXFP4, B=1, S=8192, N=65536,
                                        windows="irregular", w_fmt=W_F32, seed=4,
                                        group_rows=True),
+    # The DeepGEMM MX reproducer's shapes (window [0, N - S + i)), for a
+    # like-for-like reading of its published times.
+    "mxfp8_2048x32768": dict(fmt=FMT_MXFP8, B=1, S=2048, N=32768,
+                             windows="causal_excl", w_fmt=W_F32, seed=5),
+    "mxfp4_2048x32768": dict(fmt=FMT_MXFP4, B=1, S=2048, N=32768,
+                             windows="causal_excl", w_fmt=W_F32, seed=6),
+    "mxfp4_8192x65536": dict(fmt=FMT_MXFP4, B=1, S=8192, N=65536,
+                             windows="causal_excl", w_fmt=W_F32, seed=7),
 }
 
 

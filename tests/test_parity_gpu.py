@@ -203,7 +203,10 @@ def sample_rows(B, S, step):
 @pytest.mark.parametrize("name,step", [("bf16_batched_causal_4096", 256),
                                        ("fp8_per_token_2048x32768", 256),
                                        ("mxfp8_8192x65536", 512),
-                                       ("mxfp4_irregular_8192x65536", 512)])
+                                       ("mxfp4_irregular_8192x65536", 512),
+                                       ("mxfp8_2048x32768", 256),
+                                       ("mxfp4_2048x32768", 256),
+                                       ("mxfp4_8192x65536", 1024)])
 def test_full_size_workload(name, step):
     case = synth.make_workload(name)
     t = binding.case_to_device(case)
