@@ -180,6 +180,17 @@ IDX_API int indexer_get_last_error(idx_stream_t stream);
  * below 1e6 are raised to 1e6. Returns the previous value. */
 IDX_API int64_t indexer_set_wait_limit_ns(int64_t ns);
 
+/* Failure-detection self-test (no counterpart in the method: a diagnostic
+ * of this library). Enqueues on `stream` one device-side wait of the kind the
+ * logits kernel's roles use, on a barrier that nothing arrives on, so that it
+ * runs out after `limit_ns` nanoseconds (1e3 .. 1e9, else IDX_ERR_SHAPE) and
+ * records IDX_ERR_TIMEOUT in the (device, stream) error word, as a logits call
+ * that gave up would; indexer_get_last_error(stream) then returns
+ * IDX_ERR_TIMEOUT and clears it. Nothing else is in flight, so the context
+ * stays usable. Returns IDX_OK once enqueued, IDX_ERR_DEVICE off sm_103,
+ * IDX_ERR_CUDA if allocation or launch fails. */
+IDX_API int indexer_selftest_wait_timeout(int64_t limit_ns, idx_stream_t stream);
+
 /* Number of kernel launches one indexer_logits call with this shape makes
  * (2 with IDX_FLAG_GROUP_ROWS in effect, else 1); for launch counts in
  * benchmarks. */

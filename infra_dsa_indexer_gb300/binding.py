@@ -68,6 +68,8 @@ def load():
         lib.indexer_get_last_error.argtypes = [vp]
         lib.indexer_set_wait_limit_ns.restype = i64
         lib.indexer_set_wait_limit_ns.argtypes = [i64]
+        lib.indexer_selftest_wait_timeout.restype = i32
+        lib.indexer_selftest_wait_timeout.argtypes = [i64, vp]
         lib.indexer_launches_per_call.restype = i32
         lib.indexer_launches_per_call.argtypes = [ctypes.POINTER(idx_shape)]
         lib.indexer_shutdown.restype = i32
@@ -137,6 +139,12 @@ def indexer_get_last_error(stream=None) -> int:
 
 def indexer_set_wait_limit_ns(ns: int) -> int:
     return load().indexer_set_wait_limit_ns(int(ns))
+
+
+def indexer_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    st = load().indexer_selftest_wait_timeout(int(limit_ns), _stream(stream))
+    if st != IDX_OK:
+        raise IndexerError(st, "indexer_selftest_wait_timeout")
 
 
 def indexer_launches_per_call(shape: idx_shape) -> int:

@@ -387,6 +387,24 @@ int indexer_get_last_error(idx_stream_t stream_) {
   return word == 0 ? IDX_OK : (word == dsa::kErrTimeout ? IDX_ERR_TIMEOUT : word);
 }
 
+int indexer_selftest_wait_timeout(int64_t limit_ns, idx_stream_t stream_) {
+  if (limit_ns < 1000 || limit_ns > 1000000000LL) return IDX_ERR_SHAPE;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return IDX_ERR_CUDA;
+  int32_t* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo* di = nullptr;
+    int st = get_device_info(dev, &di);
+    if (st) return st;
+    if (di->cc_major != 10 || di->cc_minor != 3) return IDX_ERR_DEVICE;
+    if ((st = get_scratch(dev, stream, kScratchInts, &scratch))) return st;
+  }
+  dsa::wait_selftest_kernel<<<1, 32, 0, stream>>>(scratch, static_cast<uint64_t>(limit_ns));
+  return cudaGetLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+}
+
 int indexer_shutdown(void) {
   std::lock_guard<std::mutex> lock(g_mutex);
   int rc = IDX_OK;

@@ -195,7 +195,8 @@ struct Layout {
   static constexpr int kSfbOff = kSfaOff + (T::kMX ? T::kStages * kSfaBytes : 0);
   static constexpr int kInfoOff = kSfbOff + (T::kMX ? 2 * kSfbBytes : 0);
   static constexpr int kBarOff = kInfoOff + 2 * (int)sizeof(UnitInfo);
-  static constexpr int kNumBars = 2 + 2 + 2 * T::kStages + 2 * kAccBufs + (T::kMX ? T::kStages : 0);
+  static constexpr int kNumBars =
+      2 + 2 + 2 * T::kStages + 2 * kAccBufs + (T::kMX ? T::kStages : 0) + 1;
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
   static constexpr int kBytes = kMiscOff + 16;
   static_assert(kBytes <= 232448, "shared memory budget");
@@ -313,6 +314,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
   uint64_t* acc_full = k_empty + T::kStages;
   uint64_t* acc_empty = acc_full + kAccBufs;
   uint64_t* sf_full = acc_empty + kAccBufs;  // MX only
+  uint64_t* drain = sf_full + (T::kMX ? T::kStages : 0);  // MMA issuer, after an abort
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
 
@@ -339,6 +341,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       mbar_init(&k_empty[s], 1);
       if constexpr (T::kMX) mbar_init(&sf_full[s], 32);
     }
+    mbar_init(drain, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -370,7 +373,13 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       u = __shfl_sync(0xffffffffu, u, 0);
       if (!ok) {
-        if (lane == 0) raise_error(p.scratch, abort_flag, kErrTimeout);
+        if (lane == 0) {
+          raise_error(p.scratch, abort_flag, kErrTimeout);
+          // Let the Q loads (and scale copies) of the units still in the
+          // slots land before the CTA exits.
+          for (uint32_t j = it > 2 ? it - 2 : 0; j < it; ++j)
+            mbar_wait_drain(&unit_full[j & 1], (j >> 1) & 1, p.timeout_ns);
+        }
         break;
       }
       UnitInfo& in = info[slot];
@@ -533,6 +542,15 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       }
       if (lane == 0) mbar_arrive(&unit_empty[slot]);
     }
+    if (*abort_flag && lane == 0) {
+      // Let the key tiles (and scale copies) of the last kStages issues land
+      // before the CTA exits.
+      for (uint32_t j = kiter > T::kStages ? kiter - T::kStages : 0; j < kiter; ++j) {
+        mbar_wait_drain(&k_full[j % T::kStages], (j / T::kStages) & 1, p.timeout_ns);
+        if constexpr (T::kMX)
+          mbar_wait_drain(&sf_full[j % T::kStages], (j / T::kStages) & 1, p.timeout_ns);
+      }
+    }
   } else if (warp == 1 && lane == 0) {
     // --------------------------------------------------------------- MMA issuer
     uint32_t kiter = 0, aiter = 0, units_mma = 0;
@@ -620,6 +638,12 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         break;
       }
       tc_commit(&unit_empty[slot]);
+    }
+    if (*abort_flag) {
+      // A commit tracks every MMA and TMEM copy this thread issued: wait for
+      // them before the accumulator memory is freed.
+      tc_commit(drain);
+      mbar_wait_drain(drain, 0, p.timeout_ns);
     }
   } else if (warp >= kEpiWarp0) {
     // ---------------------------------------------------------------- epilogue
@@ -725,6 +749,21 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       atomicExch(p.scratch + 1, 0);
       __threadfence();
     }
+  }
+}
+
+// Diagnostic: one wait of the kind every role above uses, on a barrier that
+// nothing arrives on, so that it runs out after `timeout_ns`; it records
+// kErrTimeout in the error word exactly as a role that gives up does. Nothing
+// is in flight when the kernel returns, so the context stays usable.
+__global__ void wait_selftest_kernel(int32_t* scratch, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_word;
+  if (threadIdx.x == 0) {
+    abort_word = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait(&bar, 0, &abort_word, timeout_ns)) atomicExch(scratch + 2, kErrTimeout);
   }
 }
 

@@ -81,6 +81,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// Bounded wait that ignores the abort flag: used after an abort to let this
+// thread's own copies and MMAs in flight land before the CTA exits.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity,
+                                                uint64_t timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t start = globaltimer_ns();
+  while (globaltimer_ns() - start <= timeout_ns)
+    if (mbar_try_wait_for(bar, parity, kSuspendHintNs)) return true;
+  return false;
+}
+
 // Same contract, polling back to back: for a wait on the critical path, where
 // the wake-up delay of a suspended thread would show. The clock is read only
 // after the first few thousand polls.
