@@ -44,8 +44,13 @@ L2_FLUSH_BYTES = 256 << 20
 # workload, with the digest of the kernel sources it was taken on (see
 # profiles/). Reported as roofline.traffic only while the sources still match.
 PROFILED_TRAFFIC = {
-    "bf16_batched_causal_4096": ("f3fe3f1696969c3f", 137.508096e6 + 79.477504e6),
-    "fp8_per_token_2048x32768": ("f3fe3f1696969c3f", 21.923328e6 + 208.466176e6),
+    "bf16_batched_causal_4096": ("67f0857fb65d0ffb", 137.465088e6 + 79.895552e6),
+    "fp8_per_token_2048x32768": ("67f0857fb65d0ffb", 21.673216e6 + 207.764224e6),
+    "mxfp8_2048x32768": ("67f0857fb65d0ffb", 22.211072e6 + 208.051712e6),
+    "mxfp4_2048x32768": ("67f0857fb65d0ffb", 11.729408e6 + 208.220672e6),
+    "mxfp8_8192x65536": ("67f0857fb65d0ffb", 81478912 + 2087796480),
+    "mxfp4_8192x65536": ("67f0857fb65d0ffb", 43056128 + 2087727872),
+    "mxfp4_irregular_8192x65536": ("67f0857fb65d0ffb", 42290944 + 2086134528),
 }
 
 
