@@ -73,7 +73,7 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="bf16_batched_causal_4096")
     ap.add_argument("--e2e-steps", type=int, default=50)
-    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -201,7 +201,8 @@ def oracle_sample_rate(case, seconds, rng_seed=0):
                       rows=rows, want_den=False, nthreads=nth)
         return time.perf_counter() - t0
 
-    probe = rng.choice(total_rows, size=min(total_rows, nth), replace=False)
+    # calibrate on a probe large enough that thread start-up does not dominate
+    probe = rng.choice(total_rows, size=min(total_rows, 8 * nth), replace=False)
     dt = run(probe)
     rate = max(pairs[probe].sum(), 1) / max(dt, 1e-6)       # pairs per second
     n = int(min(total_rows, max(nth, seconds * rate / max(pairs.mean(), 1))))
