@@ -77,6 +77,8 @@ def parse_args(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--out-bf16", action="store_true",
+                    help="write the logits as BF16 (IDX_FLAG_OUT_BF16) instead of FP32")
     return ap.parse_args(argv)
 
 
@@ -273,6 +275,7 @@ def workload_config(case, args):
             "w_format": "bf16" if case.w_fmt == synth.W_BF16 else "f32",
             "in_window_pairs": case.in_window_pairs(), "clean": bool(case.clean),
             "group_rows": bool(case.group_rows),
+            "out_format": "bf16" if getattr(args, "out_bf16", False) else "f32",
             "l2": "flushed before every timed call (256 MiB write)",
             "parallelism": f"replicas x{args.gpus}"}
 
@@ -290,7 +293,7 @@ def run_ours(args, dist):
     binding.load()
     case = synth.make_workload(args.workload)
     flops = case.in_window_flops()
-    t = binding.case_to_device(case, device=f"cuda:{dev}")
+    t = binding.case_to_device(case, device=f"cuda:{dev}", out_bf16=args.out_bf16)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=f"cuda:{dev}")
     launches_per_call = binding.indexer_launches_per_call(t["shape"])
@@ -334,9 +337,9 @@ def run_ours(args, dist):
         for key in ("q", "k", "w", "ks", "ke", "q_sf", "k_sf", "k_scales"):
             if t[key] is not None:
                 host[key] = t[key].cpu().pin_memory()
-        out_host = torch.empty(t["out"].shape, dtype=torch.float32).pin_memory()
+        out_host = torch.empty(t["out"].shape, dtype=t["out"].dtype).pin_memory()
         h2d = sum(v.numel() * v.element_size() for v in host.values())
-        d2h = out_host.numel() * 4
+        d2h = out_host.numel() * out_host.element_size()
         n_e2e = max(3, min(args.e2e_steps, args.steps))
         dist.barrier()
         torch.cuda.synchronize()
@@ -361,7 +364,7 @@ def run_ours(args, dist):
     peak = peaks["bf16_tflops"] * FMT_PEAK_RATIO[case.fmt]
     achieved = flops / (ms_local * 1e-3) / 1e12
     srt = sorted(per)
-    prof = PROFILED_TRAFFIC.get(args.workload)
+    prof = None if args.out_bf16 else PROFILED_TRAFFIC.get(args.workload)
     traffic = prof[1] if prof and prof[0] == kernel_source_digest() else None
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": achieved / peak, "traffic": traffic,
@@ -369,7 +372,8 @@ def run_ours(args, dist):
                             "(nominal format ratio)" if case.fmt else f"{peak_src} bf16 burst"),
             "kernel": "dsa::indexer_logits_kernel",
             "algorithmic_flops_per_launch": flops,
-            "hbm_write_gbs": case.B * case.S * case.N * 4 / (ms_local * 1e-3) / 1e9,
+            "hbm_write_gbs": case.B * case.S * case.N * (2 if args.out_bf16 else 4)
+                             / (ms_local * 1e-3) / 1e9,
             "hbm_peak_gbs": peaks["hbm_gbs"]}
     cpu = None
     if not args.no_cpu_baseline:

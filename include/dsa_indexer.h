@@ -64,7 +64,8 @@ typedef enum idx_status {
   IDX_ERR_SHAPE = 2,       /* H != 64, D != 128, S % 4 != 0, B/S < 1, N < 1,
                               out_row_stride < N, or a size beyond int32 indexing    */
   IDX_ERR_FORMAT = 3,      /* unknown fmt / w_fmt, or scales missing for MX          */
-  IDX_ERR_ALIGN = 4,       /* q/k/w base or q/k stride not 16-byte aligned             */
+  IDX_ERR_ALIGN = 4,       /* q/k/w base or q/k stride not 16-byte aligned, or out
+                              not aligned to its element size                         */
   IDX_ERR_SCALE = 5,       /* sm_scale is not finite                                  */
   IDX_ERR_DEVICE = 6,      /* current device is not compute capability 10.3 (sm_103) */
   IDX_ERR_CUDA = 7,        /* a CUDA runtime call failed (launch, allocation, ...)   */
@@ -82,6 +83,13 @@ typedef enum idx_status {
  * indexer_logits_noalloc. The logits do not depend on it. */
 #define IDX_FLAG_GROUP_ROWS 1
 
+/* idx_shape.flags: write the logits as BF16 (round to nearest even of the
+ * FP32 result; -inf stays -inf) instead of FP32, halving the bytes stored.
+ * The output then holds BF16 elements and out_row_stride counts BF16
+ * elements. DeepGEMM's MX logits call takes the same choice as its
+ * logits_dtype argument. */
+#define IDX_FLAG_OUT_BF16 2
+
 /* Problem shape and layout. Zero strides mean "dense". */
 typedef struct idx_shape {
   int32_t B;              /* batches (uniform length), >= 1                          */
@@ -95,7 +103,7 @@ typedef struct idx_shape {
   int64_t q_row_bytes;    /* bytes between consecutive (b,i,h) rows of q; 0 = dense    */
   int64_t k_row_bytes;    /* bytes between consecutive keys of k; 0 = dense            */
   int64_t k_batch_bytes;  /* bytes between batches of k; 0 = N * k_row_bytes           */
-  int64_t out_row_stride; /* floats between consecutive output rows; 0 = N             */
+  int64_t out_row_stride; /* elements between consecutive output rows; 0 = N           */
 } idx_shape;
 
 /* Compute the logits (one call of the hot path).
@@ -122,7 +130,8 @@ typedef struct idx_shape {
  *           zero: columns of 128-key tiles that contain no in-window key of
  *           any of the row's 4-row group are left untouched; the rest is
  *           written (-inf outside the window).
- *  out      FP32 [B,S,out_row_stride]; columns >= N are never written.
+ *  out      FP32 (BF16 with IDX_FLAG_OUT_BF16) [B,S,out_row_stride], base
+ *           aligned to its element size; columns >= N are never written.
  *  shape    see idx_shape (host pointer, read during the call only).
  *  stream   CUDA stream of the launch.
  *
@@ -138,7 +147,7 @@ typedef struct idx_shape {
  */
 IDX_API int indexer_logits(const void* q, const uint8_t* q_sf, const void* k, const uint8_t* k_sf,
                    const float* k_scales, const void* w, const int32_t* ks, const int32_t* ke,
-                   float sm_scale, int clean, float* out, const idx_shape* shape,
+                   float sm_scale, int clean, void* out, const idx_shape* shape,
                    idx_stream_t stream);
 
 /* Same computation, arguments and checks as indexer_logits, but this call
@@ -163,7 +172,7 @@ IDX_API int indexer_logits(const void* q, const uint8_t* q_sf, const void* k, co
 IDX_API int indexer_logits_noalloc(const void* q, const uint8_t* q_sf, const void* k,
                                    const uint8_t* k_sf, const float* k_scales, const void* w,
                                    const int32_t* ks, const int32_t* ke, float sm_scale,
-                                   int clean, float* out, const idx_shape* shape,
+                                   int clean, void* out, const idx_shape* shape,
                                    idx_stream_t stream);
 
 /* Human-readable text for an idx_status value (static storage, never NULL). */

@@ -18,6 +18,7 @@ import torch
 IDX_FMT_BF16, IDX_FMT_E4M3, IDX_FMT_MXFP8, IDX_FMT_MXFP4 = 0, 1, 2, 3
 IDX_W_F32, IDX_W_BF16 = 0, 1
 IDX_FLAG_GROUP_ROWS = 1
+IDX_FLAG_OUT_BF16 = 2
 IDX_OK = 0
 IDX_ERR_TIMEOUT = 8
 
@@ -106,7 +107,8 @@ def indexer_logits(q, q_sf, k, k_sf, k_scales, w, ks, ke, sm_scale, clean, out,
                    shape: idx_shape, stream=None) -> None:
     """Enqueue one logits call. Tensors are CUDA tensors holding the raw
     layouts of include/dsa_indexer.h (q [B,S,H,row], k [B,N,row], w [B,S,H],
-    ks/ke [B,S] int32, out [B,S,>=N] float32); q_sf/k_sf/k_scales may be None."""
+    ks/ke [B,S] int32, out [B,S,>=N] float32, or bfloat16 with IDX_FLAG_OUT_BF16);
+    q_sf/k_sf/k_scales may be None."""
     lib = load()
     st = lib.indexer_logits(_ptr(q), _ptr(q_sf), _ptr(k), _ptr(k_sf), _ptr(k_scales), _ptr(w),
                             _ptr(ks), _ptr(ke), ctypes.c_float(sm_scale), int(bool(clean)),
@@ -163,8 +165,9 @@ def indexer_version() -> int:
 # convenience: a synth.Case on the device
 # ---------------------------------------------------------------------------
 
-def case_to_device(case, device="cuda", out_row_stride=None):
-    """Copy a synth.Case's input bytes to `device`; allocate the FP32 output."""
+def case_to_device(case, device="cuda", out_row_stride=None, out_bf16=False):
+    """Copy a synth.Case's input bytes to `device`; allocate the FP32 (or,
+    with out_bf16, BF16) output."""
     def dev(a):
         if a is None:
             return None
@@ -174,10 +177,11 @@ def case_to_device(case, device="cuda", out_row_stride=None):
     t = dict(q=dev(case.q), k=dev(case.k), w=dev(case.w), ks=dev(case.ks), ke=dev(case.ke),
              q_sf=dev(case.q_sf), k_sf=dev(case.k_sf), k_scales=dev(case.k_tok))
     stride = out_row_stride or case.N
-    t["out"] = torch.empty((case.B, case.S, stride), dtype=torch.float32, device=device)
+    t["out"] = torch.empty((case.B, case.S, stride),
+                           dtype=torch.bfloat16 if out_bf16 else torch.float32, device=device)
+    flags = (IDX_FLAG_GROUP_ROWS if case.group_rows else 0) | (IDX_FLAG_OUT_BF16 if out_bf16 else 0)
     t["shape"] = make_shape(case.B, case.S, case.N, case.H, case.D, case.fmt, case.w_fmt,
-                            out_row_stride=stride,
-                            flags=IDX_FLAG_GROUP_ROWS if case.group_rows else 0)
+                            out_row_stride=stride, flags=flags)
     return t
 
 

@@ -26,7 +26,7 @@ struct DeviceInfo {
   bool valid = false;
   int sm_count = 0;
   int cc_major = 0, cc_minor = 0;
-  bool smem_set[8] = {false, false, false, false, false, false, false, false};
+  bool smem_set[16] = {};  // per kernel instantiation (format, sign, output type)
   bool plan_attr_set = false;
 };
 
@@ -160,11 +160,11 @@ int encode_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, in
   return r == CUDA_SUCCESS ? IDX_OK : IDX_ERR_CUDA;
 }
 
-template <int FMT, bool NEG_EPI>
-int launch(const KernelParams& prm, int grid, DeviceInfo* di, cudaStream_t stream) {
+template <int FMT, bool NEG_EPI, bool OUT_BF16>
+int launch_kernel(const KernelParams& prm, int grid, DeviceInfo* di, cudaStream_t stream) {
   constexpr int smem = dsa::Layout<FMT>::kBytes;
-  auto kern = dsa::indexer_logits_kernel<FMT, NEG_EPI>;
-  bool& attr_set = di->smem_set[FMT * 2 + (NEG_EPI ? 1 : 0)];
+  auto kern = dsa::indexer_logits_kernel<FMT, NEG_EPI, OUT_BF16>;
+  bool& attr_set = di->smem_set[FMT * 4 + (NEG_EPI ? 2 : 0) + (OUT_BF16 ? 1 : 0)];
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
@@ -173,6 +173,12 @@ int launch(const KernelParams& prm, int grid, DeviceInfo* di, cudaStream_t strea
   }
   kern<<<grid, dsa::Layout<FMT>::kThreads, smem, stream>>>(prm);
   return cudaGetLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+}
+
+template <int FMT, bool NEG_EPI>
+int launch(const KernelParams& prm, int grid, DeviceInfo* di, cudaStream_t stream) {
+  return prm.out_bf16 ? launch_kernel<FMT, NEG_EPI, true>(prm, grid, di, stream)
+                      : launch_kernel<FMT, NEG_EPI, false>(prm, grid, di, stream);
 }
 
 }  // namespace
@@ -191,7 +197,9 @@ const char* indexer_status_string(int status) {
     case IDX_ERR_NULL: return "a required pointer is NULL";
     case IDX_ERR_SHAPE: return "unsupported or inconsistent shape (H must be 64, D 128, S % 4 == 0, N >= 1, out_row_stride >= N)";
     case IDX_ERR_FORMAT: return "unknown format, or scales missing/present for the wrong format";
-    case IDX_ERR_ALIGN: return "q/k/w base address or q/k stride is not 16-byte aligned";
+    case IDX_ERR_ALIGN:
+      return "q/k/w base address or q/k stride is not 16-byte aligned, or out is not aligned "
+             "to its element size";
     case IDX_ERR_SCALE: return "sm_scale is not finite";
     case IDX_ERR_DEVICE: return "current device is not compute capability 10.3 (sm_103)";
     case IDX_ERR_CUDA: return "a CUDA runtime call failed";
@@ -218,7 +226,7 @@ namespace {
 // use) or selects the no-allocation variant's fixed device array.
 int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint8_t* k_sf,
                    const float* k_scales, const void* w, const int32_t* ks, const int32_t* ke,
-                   float sm_scale, int clean, float* out, const idx_shape* shape,
+                   float sm_scale, int clean, void* out, const idx_shape* shape,
                    cudaStream_t stream, bool fixed_scratch) {
   if (!shape || !q || !k || !w || !ks || !ke || !out) return IDX_ERR_NULL;
   const idx_shape sh = *shape;
@@ -228,7 +236,7 @@ int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
   if (mx && (!q_sf || !k_sf)) return IDX_ERR_NULL;
   if (!mx && (q_sf || k_sf)) return IDX_ERR_FORMAT;
   if (k_scales && sh.fmt != IDX_FMT_E4M3) return IDX_ERR_FORMAT;
-  if (sh.H != dsa::kHeads || sh.D != dsa::kHeadDim || (sh.flags & ~IDX_FLAG_GROUP_ROWS) != 0)
+  if (sh.H != dsa::kHeads || sh.D != dsa::kHeadDim || (sh.flags & ~(IDX_FLAG_GROUP_ROWS | IDX_FLAG_OUT_BF16)) != 0)
     return IDX_ERR_SHAPE;
   if (sh.B < 1 || sh.S < 1 || sh.S % dsa::kRowsPerBlock != 0 || sh.N < 1) return IDX_ERR_SHAPE;
   if (!std::isfinite(sm_scale)) return IDX_ERR_SCALE;
@@ -250,6 +258,8 @@ int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
     return IDX_ERR_ALIGN;
   if (mx && ((reinterpret_cast<uintptr_t>(q_sf) & 3u) || (reinterpret_cast<uintptr_t>(k_sf) & 3u)))
     return IDX_ERR_ALIGN;
+  const bool out_bf16 = (sh.flags & IDX_FLAG_OUT_BF16) != 0;
+  if (reinterpret_cast<uintptr_t>(out) & (out_bf16 ? 1u : 3u)) return IDX_ERR_ALIGN;
 
   std::lock_guard<std::mutex> lock(g_mutex);
   int dev = 0;
@@ -299,6 +309,7 @@ int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
   prm.ks = ks;
   prm.ke = ke;
   prm.out = out;
+  prm.out_bf16 = out_bf16 ? 1 : 0;
   prm.scratch = scratch;
   prm.out_row_stride = out_stride;
   prm.B = sh.B;
@@ -346,7 +357,7 @@ extern "C" {
 
 int indexer_logits(const void* q, const uint8_t* q_sf, const void* k, const uint8_t* k_sf,
                    const float* k_scales, const void* w, const int32_t* ks, const int32_t* ke,
-                   float sm_scale, int clean, float* out, const idx_shape* shape,
+                   float sm_scale, int clean, void* out, const idx_shape* shape,
                    idx_stream_t stream) {
   return enqueue_logits(q, q_sf, k, k_sf, k_scales, w, ks, ke, sm_scale, clean, out, shape,
                         reinterpret_cast<cudaStream_t>(stream), false);
@@ -355,7 +366,7 @@ int indexer_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
 int indexer_logits_noalloc(const void* q, const uint8_t* q_sf, const void* k,
                            const uint8_t* k_sf, const float* k_scales, const void* w,
                            const int32_t* ks, const int32_t* ke, float sm_scale, int clean,
-                           float* out, const idx_shape* shape, idx_stream_t stream) {
+                           void* out, const idx_shape* shape, idx_stream_t stream) {
   // One call needs kScratchWordsPerCall words whatever the shape; refuse
   // anything that would need more than the fixed array holds.
   if (kScratchWordsPerCall > kFixedScratchWords) return IDX_ERR_SCRATCH;

@@ -95,11 +95,12 @@ struct KernelParams {
   const int32_t* ks;
   const int32_t* ke;
   const int32_t* perm;  // [B,S] row order within each batch, or null (identity)
-  float* out;
+  void* out;         // FP32, or BF16 when out_bf16
   int32_t* scratch;  // [0] unit counter, [1] finished CTAs, [2] error word
   int64_t out_row_stride;
   int32_t B, S, N;
   int32_t w_bf16;
+  int32_t out_bf16;  // selects the OUT_BF16 instantiation
   int32_t clean;
   int32_t num_units;
   int32_t nchunk;
@@ -211,11 +212,17 @@ __device__ __forceinline__ void raise_error(int32_t* scratch, volatile int* abor
   atomicExch(scratch + 2, code);
 }
 
-// Write -inf to columns [a, b) of one output row; the 128 threads of the
-// four warps sharing `row` cover 128 consecutive columns per step.
-__device__ __forceinline__ void fill_neg_inf(float* row, int a, int b, int tid128) {
-  const float ninf = __int_as_float(0xff800000);
-  for (int j = a + tid128; j < b; j += 128) __stcs(row + j, ninf);
+// Write -inf to columns [a, b) of one output row (FP32, or BF16 0xff80);
+// the 128 threads of the four warps sharing `row` cover 128 consecutive
+// columns per step.
+__device__ __forceinline__ void fill_neg_inf(char* row, int a, int b, int tid128, bool bf16) {
+  if (bf16) {
+    for (int j = a + tid128; j < b; j += 128) st_cs_b16(row + 2 * static_cast<int64_t>(j), 0xff80);
+  } else {
+    const float ninf = __int_as_float(0xff800000);
+    float* rowf = reinterpret_cast<float*>(row);
+    for (int j = a + tid128; j < b; j += 128) __stcs(rowf + j, ninf);
+  }
 }
 
 // sum_h w[h] * R(x[h]) over the 64 heads of a row, R(x) = max(x, 0) (NEG:
@@ -290,7 +297,8 @@ __device__ __forceinline__ void mma_step(uint32_t d_tmem, uint64_t a_desc, uint6
 
 // NEG_EPI: the epilogue applies a negative sm_scale itself (MXFP4, whose MMA
 // kind has no negate bit); every other case negates the MMA's A operand.
-template <int FMT, bool NEG_EPI>
+// OUT_BF16: the logits are stored as BF16 (round to nearest even).
+template <int FMT, bool NEG_EPI, bool OUT_BF16>
 __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
     indexer_logits_kernel(const __grid_constant__ KernelParams p) {
   using T = Traits<FMT>;
@@ -665,17 +673,19 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       if (in.stop) break;
       const int b = in.b, c0 = in.c0, c1 = in.c1, t0 = in.t0, t1 = in.t1, flags = in.flags;
       int lo[R], hi[R];
-      float* orow[R];
+      char* orow[R];
+      constexpr bool obf = OUT_BF16;
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         lo[r] = in.lo[r0 + r];
         hi[r] = in.hi[r0 + r];
-        orow[r] = p.out + static_cast<int64_t>(in.row[r0 + r]) * p.out_row_stride;
+        orow[r] = static_cast<char*>(p.out) +
+                  static_cast<int64_t>(in.row[r0 + r]) * p.out_row_stride * (obf ? 2 : 4);
       }
       const float* wrows = reinterpret_cast<const float*>(wbuf + slot * L::kWBytes) + r0 * kHeads;
       if (p.clean && (flags & 1)) {
 #pragma unroll
-        for (int r = 0; r < R; ++r) fill_neg_inf(orow[r], 0, t0 * kKeysPerTile, tid128);
+        for (int r = 0; r < R; ++r) fill_neg_inf(orow[r], 0, t0 * kKeysPerTile, tid128, obf);
       }
       // Per-key scale (E4M3), loaded one tile ahead so that its latency
       // overlaps the previous tile instead of stalling the loop head.
@@ -716,8 +726,13 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         for (int r = 0; r < R; ++r) sums[r] = racc[r].total();
         if (j < p.N) {
 #pragma unroll
-          for (int r = 0; r < R; ++r)
-            __stcs(orow[r] + j, (j >= lo[r] && j < hi[r]) ? sums[r] * (sm_abs * kscale) : ninf);
+          for (int r = 0; r < R; ++r) {
+            const float v = (j >= lo[r] && j < hi[r]) ? sums[r] * (sm_abs * kscale) : ninf;
+            if (obf)
+              st_cs_b16(orow[r] + 2 * static_cast<int64_t>(j), f32_to_bf16_rn(v));
+            else
+              __stcs(reinterpret_cast<float*>(orow[r]) + j, v);
+          }
         }
       }
       if (!ok) {
@@ -726,7 +741,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       }
       if (p.clean && (flags & 2)) {
 #pragma unroll
-        for (int r = 0; r < R; ++r) fill_neg_inf(orow[r], t1 * kKeysPerTile, p.N, tid128);
+        for (int r = 0; r < R; ++r) fill_neg_inf(orow[r], t1 * kKeysPerTile, p.N, tid128, obf);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&unit_empty[slot]);

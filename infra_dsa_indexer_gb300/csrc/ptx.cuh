@@ -49,6 +49,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Streaming (evict-first) 2-byte store, and FP32 -> BF16 round to nearest
+// even (the PTX conversion; infinities are kept).
+__device__ __forceinline__ void st_cs_b16(void* p, uint16_t v) {
+  asm volatile("st.global.cs.b16 [%0], %1;" ::"l"(p), "h"(v) : "memory");
+}
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float x) {
+  uint16_t r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(x));
+  return r;
+}
+
 // try_wait with a suspend-time hint: if the phase is still open the thread is
 // suspended until it completes or about `ns` nanoseconds pass.
 __device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, uint32_t parity, uint32_t ns) {

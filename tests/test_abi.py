@@ -78,7 +78,9 @@ def shp(**kw):
     ({}, dict(S=6), 2),
     ({}, dict(N=0), 2),
     ({}, dict(B=0), 2),
-    ({}, dict(flags=2), 2),                               # unknown flag bit
+    ({}, dict(flags=4), 2),                               # unknown flag bit
+    (dict(out=ctypes.c_void_p(0x1002)), {}, 4),           # FP32 out not 4-byte aligned
+    (dict(out=ctypes.c_void_p(0x1001)), dict(flags=2), 4),  # BF16 out not 2-byte aligned
     ({}, dict(out_row_stride=50), 2),
     ({}, dict(fmt=7), 3),
     ({}, dict(w_fmt=3), 3),
