@@ -61,8 +61,8 @@ typedef enum idx_w_format { IDX_W_F32 = 0, IDX_W_BF16 = 1 } idx_w_format;
 typedef enum idx_status {
   IDX_OK = 0,
   IDX_ERR_NULL = 1,        /* a required pointer is NULL                            */
-  IDX_ERR_SHAPE = 2,       /* H != 64, D != 128, S % 4 != 0, B/S < 1, N < 1,
-                              out_row_stride < N, or a size beyond int32 indexing    */
+  IDX_ERR_SHAPE = 2,       /* H != 64, D != 128, B/S/N < 1, out_row_stride < N, or a
+                              size beyond int32 indexing                              */
   IDX_ERR_FORMAT = 3,      /* unknown fmt / w_fmt, or scales missing for MX          */
   IDX_ERR_ALIGN = 4,       /* q/k/w base or q/k stride not 16-byte aligned, or out
                               not aligned to its element size                         */
@@ -93,7 +93,7 @@ typedef enum idx_status {
 /* Problem shape and layout. Zero strides mean "dense". */
 typedef struct idx_shape {
   int32_t B;              /* batches (uniform length), >= 1                          */
-  int32_t S;              /* query rows per batch, multiple of 4                      */
+  int32_t S;              /* query rows per batch, >= 1                               */
   int32_t N;              /* keys per batch, >= 1                                      */
   int32_t H;              /* query heads, must be 64                                   */
   int32_t D;              /* head dimension, must be 128                               */

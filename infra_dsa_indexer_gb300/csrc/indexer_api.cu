@@ -195,7 +195,7 @@ const char* indexer_status_string(int status) {
   switch (status) {
     case IDX_OK: return "ok";
     case IDX_ERR_NULL: return "a required pointer is NULL";
-    case IDX_ERR_SHAPE: return "unsupported or inconsistent shape (H must be 64, D 128, S % 4 == 0, N >= 1, out_row_stride >= N)";
+    case IDX_ERR_SHAPE: return "unsupported or inconsistent shape (H must be 64, D 128, B, S, N >= 1, out_row_stride >= N)";
     case IDX_ERR_FORMAT: return "unknown format, or scales missing/present for the wrong format";
     case IDX_ERR_ALIGN:
       return "q/k/w base address or q/k stride is not 16-byte aligned, or out is not aligned "
@@ -238,7 +238,7 @@ int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
   if (k_scales && sh.fmt != IDX_FMT_E4M3) return IDX_ERR_FORMAT;
   if (sh.H != dsa::kHeads || sh.D != dsa::kHeadDim || (sh.flags & ~(IDX_FLAG_GROUP_ROWS | IDX_FLAG_OUT_BF16)) != 0)
     return IDX_ERR_SHAPE;
-  if (sh.B < 1 || sh.S < 1 || sh.S % dsa::kRowsPerBlock != 0 || sh.N < 1) return IDX_ERR_SHAPE;
+  if (sh.B < 1 || sh.S < 1 || sh.N < 1) return IDX_ERR_SHAPE;
   if (!std::isfinite(sm_scale)) return IDX_ERR_SCALE;
 
   const int64_t elem_row_bytes =
@@ -318,13 +318,13 @@ int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
   prm.w_bf16 = sh.w_fmt == IDX_W_BF16;
   prm.clean = clean != 0;
   prm.sm_scale = sm_scale;
-  prm.blocks_per_batch = sh.S / dsa::kRowsPerBlock;
+  prm.blocks_per_batch = (sh.S + dsa::kRowsPerBlock - 1) / dsa::kRowsPerBlock;
   prm.timeout_ns = static_cast<uint64_t>(g_wait_limit_ns);
 
   // Units: every row-block split into nchunk pieces of its key tiles. Long
   // rows get pieces of at most ~64 tiles (load balance across the persistent
   // grid); small problems get enough pieces for about two per SM.
-  const int64_t row_blocks = total_rows / dsa::kRowsPerBlock;
+  const int64_t row_blocks = static_cast<int64_t>(sh.B) * prm.blocks_per_batch;
   const int64_t tiles_max = (sh.N + dsa::kKeysPerTile - 1) / dsa::kKeysPerTile;
   int64_t nchunk = (tiles_max + 63) / 64;
   const int64_t want = (2 * di->sm_count + row_blocks - 1) / row_blocks;

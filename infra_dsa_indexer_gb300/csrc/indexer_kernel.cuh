@@ -77,7 +77,7 @@ enum : int { kErrTimeout = 8, kErrAlign = 4 };
 struct UnitInfo {
   int32_t stop;
   int32_t b;
-  int32_t row[4];    // flattened row ids b*S + i of the block's rows
+  int32_t row[4];    // flattened row ids b*S + i of the block's rows; -1: no such row
   int32_t c0, c1;    // key tiles [c0, c1) computed by this unit
   int32_t t0, t1;    // key tiles [t0, t1) covered by the whole row-block
   int32_t flags;     // bit 0: fill [0, t0*128) with -inf; bit 1: fill [t1*128, N)
@@ -104,7 +104,7 @@ struct KernelParams {
   int32_t clean;
   int32_t num_units;
   int32_t nchunk;
-  int32_t blocks_per_batch;  // S / 4
+  int32_t blocks_per_batch;  // ceil(S / 4); the last block of a batch may be partial
   float sm_scale;
   uint64_t timeout_ns;
 };
@@ -406,10 +406,13 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       const int blk = p.blocks_per_batch - 1 - order / p.B;
       const int b = order % p.B;
       // The block's rows: positions 4*blk .. 4*blk+3 of the batch's row order.
+      // Positions past S (a partial last block) read the batch's last row in
+      // that order, so every address stays valid; the row gets an empty
+      // window and is never stored.
       int grow[kRowsPerBlock];
 #pragma unroll
       for (int r = 0; r < kRowsPerBlock; ++r) {
-        const int pos = blk * kRowsPerBlock + r;
+        const int pos = min(blk * kRowsPerBlock + r, p.S - 1);
         grow[r] = b * p.S + (p.perm != nullptr ? __ldg(p.perm + b * p.S + pos) : pos);
       }
       // head weights of the 4 rows -> FP32 in shared memory, row-major 4 x 64
@@ -453,9 +456,10 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         int lo_all = p.N, hi_all = 0;
 #pragma unroll
         for (int r = 0; r < kRowsPerBlock; ++r) {
-          const int lo = clampi(__ldg(p.ks + grow[r]), 0, p.N);
-          const int hi = clampi(__ldg(p.ke + grow[r]), 0, p.N);
-          in.row[r] = grow[r];
+          const bool exists = blk * kRowsPerBlock + r < p.S;
+          const int lo = exists ? clampi(__ldg(p.ks + grow[r]), 0, p.N) : 0;
+          const int hi = exists ? clampi(__ldg(p.ke + grow[r]), 0, p.N) : 0;
+          in.row[r] = exists ? grow[r] : -1;
           in.lo[r] = lo;
           in.hi[r] = hi;
           if (lo < hi) {
@@ -673,19 +677,22 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       if (in.stop) break;
       const int b = in.b, c0 = in.c0, c1 = in.c1, t0 = in.t0, t1 = in.t1, flags = in.flags;
       int lo[R], hi[R];
-      char* orow[R];
+      char* orow[R];  // null for a row past S (nothing is stored for it)
       constexpr bool obf = OUT_BF16;
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         lo[r] = in.lo[r0 + r];
         hi[r] = in.hi[r0 + r];
-        orow[r] = static_cast<char*>(p.out) +
-                  static_cast<int64_t>(in.row[r0 + r]) * p.out_row_stride * (obf ? 2 : 4);
+        const int row = in.row[r0 + r];
+        orow[r] = row < 0 ? nullptr
+                          : static_cast<char*>(p.out) +
+                                static_cast<int64_t>(row) * p.out_row_stride * (obf ? 2 : 4);
       }
       const float* wrows = reinterpret_cast<const float*>(wbuf + slot * L::kWBytes) + r0 * kHeads;
       if (p.clean && (flags & 1)) {
 #pragma unroll
-        for (int r = 0; r < R; ++r) fill_neg_inf(orow[r], 0, t0 * kKeysPerTile, tid128, obf);
+        for (int r = 0; r < R; ++r)
+          if (orow[r] != nullptr) fill_neg_inf(orow[r], 0, t0 * kKeysPerTile, tid128, obf);
       }
       // Per-key scale (E4M3), loaded one tile ahead so that its latency
       // overlaps the previous tile instead of stalling the loop head.
@@ -727,6 +734,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         if (j < p.N) {
 #pragma unroll
           for (int r = 0; r < R; ++r) {
+            if (orow[r] == nullptr) continue;
             const float v = (j >= lo[r] && j < hi[r]) ? sums[r] * (sm_abs * kscale) : ninf;
             if (obf)
               st_cs_b16(orow[r] + 2 * static_cast<int64_t>(j), f32_to_bf16_rn(v));
@@ -741,7 +749,8 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       }
       if (p.clean && (flags & 2)) {
 #pragma unroll
-        for (int r = 0; r < R; ++r) fill_neg_inf(orow[r], t1 * kKeysPerTile, p.N, tid128, obf);
+        for (int r = 0; r < R; ++r)
+          if (orow[r] != nullptr) fill_neg_inf(orow[r], t1 * kKeysPerTile, p.N, tid128, obf);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&unit_empty[slot]);

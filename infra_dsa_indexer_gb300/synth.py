@@ -153,17 +153,38 @@ def irregular_windows(rng, B, S, N, forced_empty=FORCED_EMPTY_ROWS):
     return ks.astype(np.int32), (ks + ln).astype(np.int32)
 
 
+def thd_windows(seqlens_q, seqlens_k, causal=True):
+    """Windows of sequences packed along the row and key axes of one batch
+    (the THD layout: cu_seqlens are the prefix sums of the lengths). Query
+    row i of sequence s sees that sequence's keys only: [cu_k[s], cu_k[s] +
+    n_k - n_q + i + 1) when causal (the last query row sees every key of its
+    sequence), else [cu_k[s], cu_k[s] + n_k). Returns ks, ke as int32 [1, T_q]."""
+    ks, ke = [], []
+    k0 = 0
+    for nq, nk in zip(seqlens_q, seqlens_k):
+        i = np.arange(nq, dtype=np.int64)
+        ks.append(np.full(nq, k0, dtype=np.int64))
+        ln = np.clip(nk - nq + i + 1, 0, nk) if causal else np.full(nq, nk, dtype=np.int64)
+        ke.append(k0 + ln)
+        k0 += nk
+    return (np.concatenate(ks).astype(np.int32)[None, :],
+            np.concatenate(ke).astype(np.int32)[None, :])
+
+
 # ----------------------------------------------------------------------------
 # case builder
 # ----------------------------------------------------------------------------
 
 def make_case(fmt, B, S, N, H=64, D=128, *, seed=0, windows="full",
               w_fmt=W_F32, w_std=1.0 / 8.0, sm_scale=None, ks=None, ke=None,
-              zero=False, name=None, mx_unit_scales=False, group_rows=False) -> Case:
+              zero=False, name=None, mx_unit_scales=False, group_rows=False,
+              thd=None) -> Case:
     """Draw Q, K ~ N(0,1), W ~ N(0, w_std^2), quantise to `fmt`.
 
     windows: "full" ([0,N)), "causal" ([0, N-S+i+1)), "causal_excl"
-    ([0, N-S+i)), "irregular" (random, see irregular_windows), or give ks/ke.
+    ([0, N-S+i)), "irregular" (random, see irregular_windows), "thd" (packed
+    sequences, thd = (seqlens_q, seqlens_k) summing to S and N; see
+    thd_windows), or give ks/ke.
     zero=True makes all-zero Q/K/W (MX scales = 1), as in the pages' timing
     workload."""
     rng = np.random.Generator(np.random.PCG64(seed))
@@ -214,6 +235,11 @@ def make_case(fmt, B, S, N, H=64, D=128, *, seed=0, windows="full",
             ks, ke = causal_windows(B, S, N, N - S)
         elif windows == "irregular":
             ks, ke = irregular_windows(rng, B, S, N)
+        elif windows == "thd":
+            lq, lk = thd
+            if B != 1 or sum(lq) != S or sum(lk) != N:
+                raise ValueError("thd: one batch, lengths summing to S and N")
+            ks, ke = thd_windows(lq, lk)
         else:
             raise ValueError(windows)
     ks = np.ascontiguousarray(np.broadcast_to(np.asarray(ks, dtype=np.int32), (B, S)))
@@ -245,6 +271,11 @@ WORKLOADS = {
                              windows="causal_excl", w_fmt=W_F32, seed=6),
     "mxfp4_8192x65536": dict(fmt=FMT_MXFP4, B=1, S=8192, N=65536,
                              windows="causal_excl", w_fmt=W_F32, seed=7),
+    # Three causal sequences packed along rows and keys (THD), 4 keys per
+    # query, 8192 query rows in all; the output has global key columns.
+    "thd_bf16_3seq_8192x32768": dict(fmt=FMT_BF16, B=1, S=8192, N=32768, windows="thd",
+                                     thd=((4096, 2560, 1536), (16384, 10240, 6144)),
+                                     w_fmt=W_F32, seed=8),
 }
 
 

@@ -75,7 +75,7 @@ def shp(**kw):
     (dict(out=None), {}, 1),
     ({}, dict(H=32), 2),
     ({}, dict(D=64), 2),
-    ({}, dict(S=6), 2),
+    ({}, dict(S=0), 2),
     ({}, dict(N=0), 2),
     ({}, dict(B=0), 2),
     ({}, dict(flags=4), 2),                               # unknown flag bit

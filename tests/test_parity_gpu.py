@@ -200,13 +200,42 @@ def sample_rows(B, S, step):
     return np.array(sorted(rows), dtype=np.int64)
 
 
+@pytest.mark.parametrize("S", [1, 2, 3, 5, 7, 13, 130])
+@pytest.mark.parametrize("fmt", ALL)
+def test_partial_last_row_block(S, fmt):
+    # S not a multiple of the 4-row block: the missing rows of the last block
+    # are computed on valid addresses and never stored; extra rows of the
+    # output buffer past B*S keep their sentinel.
+    B, N = 2, 333
+    case = synth.make_case(fmt, B, S, N, seed=100 + 7 * S + fmt, windows="irregular",
+                           group_rows=(S % 2 == 1))
+    t = binding.case_to_device(case)
+    big = torch.full((B * S + 4, N), 5.0, dtype=torch.float32, device="cuda")
+    t["out"] = big[: B * S].view(B, S, N)
+    binding.run_case(case, t)
+    torch.cuda.synchronize()
+    assert binding.indexer_get_last_error() == binding.IDX_OK
+    assert torch.all(big[B * S:] == 5.0)
+    ref, den = oracle_rows(case)
+    compare(big[: B * S].cpu().numpy(), ref, den)
+
+
+@pytest.mark.parametrize("fmt", ALL)
+def test_thd_packed_sequences(fmt):
+    lq, lk = (37, 64, 9), (100, 256, 40)
+    case = synth.make_case(fmt, 1, sum(lq), sum(lk), seed=120 + fmt, windows="thd",
+                           thd=(lq, lk))
+    check_full(case)
+
+
 @pytest.mark.parametrize("name,step", [("bf16_batched_causal_4096", 256),
                                        ("fp8_per_token_2048x32768", 256),
                                        ("mxfp8_8192x65536", 512),
                                        ("mxfp4_irregular_8192x65536", 512),
                                        ("mxfp8_2048x32768", 256),
                                        ("mxfp4_2048x32768", 256),
-                                       ("mxfp4_8192x65536", 1024)])
+                                       ("mxfp4_8192x65536", 1024),
+                                       ("thd_bf16_3seq_8192x32768", 256)])
 def test_full_size_workload(name, step):
     case = synth.make_workload(name)
     t = binding.case_to_device(case)
