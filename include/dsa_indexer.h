@@ -175,6 +175,42 @@ IDX_API int indexer_logits_noalloc(const void* q, const uint8_t* q_sf, const voi
                                    int clean, void* out, const idx_shape* shape,
                                    idx_stream_t stream);
 
+/* Keys in a paged cache (decode-time KV caches): key j of batch b is row
+ * j % page_size of page block_table[b * table_stride + j / page_size]. The
+ * pages need not be contiguous or in order, and batches may share pages. */
+typedef struct idx_paged {
+  const int32_t* block_table; /* device, [B, table_stride] int32 page numbers; entries
+                                 for keys < N must lie in [0, num_pages) (others are
+                                 clamped on the device: wrong values, no fault)      */
+  int32_t table_stride;       /* entries per batch, >= ceil(N / page_size)             */
+  int32_t page_size;          /* keys per page, a positive multiple of 64              */
+  int32_t num_pages;          /* pages in the cache; num_pages * page_size < 2^31      */
+  int32_t reserved;           /* must be 0                                             */
+} idx_paged;
+
+/* indexer_logits with the keys in a paged cache (no counterpart signature on
+ * the pages, which only name DeepGEMM's paged MQA-logits path and its
+ * tests). Arguments as for indexer_logits except:
+ *  k_cache        [num_pages, page_size, D] elements (MXFP4: D/2 bytes per
+ *                 key), row stride shape->k_row_bytes (0 = dense), base
+ *                 16-byte aligned; shape->k_batch_bytes must be 0.
+ *  k_sf_cache     MX formats: E8M0 [num_pages, page_size, D/32]; else NULL.
+ *  k_scales_cache IDX_FMT_E4M3: FP32 [num_pages, page_size] per-key scales or
+ *                 NULL; NULL for the other formats.
+ *  shape->N       keys per batch seen through the table (the longest
+ *                 context); each row's window [ks, ke) selects its keys, e.g.
+ *                 [0, context_len - next_n + t + 1) for decode token t.
+ *  paged          host pointer, read during the call only.
+ * Returns IDX_ERR_NULL for a NULL paged/block_table, IDX_ERR_SHAPE for a bad
+ * page size, table stride, page count or a non-zero k_batch_bytes; otherwise
+ * as indexer_logits. The logits equal those of indexer_logits on the keys
+ * gathered into a contiguous [B, N] array, bit for bit. */
+IDX_API int indexer_paged_logits(const void* q, const uint8_t* q_sf, const void* k_cache,
+                                 const uint8_t* k_sf_cache, const float* k_scales_cache,
+                                 const void* w, const int32_t* ks, const int32_t* ke,
+                                 float sm_scale, int clean, void* out, const idx_shape* shape,
+                                 const idx_paged* paged, idx_stream_t stream);
+
 /* Human-readable text for an idx_status value (static storage, never NULL). */
 IDX_API const char* indexer_status_string(int status);
 

@@ -42,6 +42,12 @@ class idx_shape(ctypes.Structure):
                 ("k_batch_bytes", ctypes.c_int64), ("out_row_stride", ctypes.c_int64)]
 
 
+class idx_paged(ctypes.Structure):
+    _fields_ = [("block_table", ctypes.c_void_p), ("table_stride", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
 def library_path() -> str:
     return _LIB_PATH
 
@@ -69,6 +75,9 @@ def load():
         lib.indexer_get_last_error.argtypes = [vp]
         lib.indexer_set_wait_limit_ns.restype = i64
         lib.indexer_set_wait_limit_ns.argtypes = [i64]
+        lib.indexer_paged_logits.restype = i32
+        lib.indexer_paged_logits.argtypes = lib.indexer_logits.argtypes[:12] + [
+            ctypes.POINTER(idx_paged), vp]
         lib.indexer_selftest_wait_timeout.restype = i32
         lib.indexer_selftest_wait_timeout.argtypes = [i64, vp]
         lib.indexer_launches_per_call.restype = i32
@@ -143,6 +152,23 @@ def indexer_set_wait_limit_ns(ns: int) -> int:
     return load().indexer_set_wait_limit_ns(int(ns))
 
 
+def indexer_paged_logits(q, q_sf, k_cache, k_sf_cache, k_scales_cache, w, ks, ke, sm_scale,
+                         clean, out, shape: idx_shape, block_table, page_size: int,
+                         num_pages: int, table_stride: int, stream=None) -> None:
+    """indexer_logits with the keys in a page cache (see idx_paged in
+    include/dsa_indexer.h): k_cache [num_pages, page_size, row bytes],
+    block_table [B, table_stride] int32, all CUDA tensors."""
+    lib = load()
+    pg = idx_paged(ctypes.c_void_p(_ptr(block_table).value if block_table is not None else None),
+                   int(table_stride), int(page_size), int(num_pages), 0)
+    st = lib.indexer_paged_logits(_ptr(q), _ptr(q_sf), _ptr(k_cache), _ptr(k_sf_cache),
+                                  _ptr(k_scales_cache), _ptr(w), _ptr(ks), _ptr(ke),
+                                  ctypes.c_float(sm_scale), int(bool(clean)), _ptr(out),
+                                  ctypes.byref(shape), ctypes.byref(pg), _stream(stream))
+    if st != IDX_OK:
+        raise IndexerError(st, "indexer_paged_logits")
+
+
 def indexer_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
     st = load().indexer_selftest_wait_timeout(int(limit_ns), _stream(stream))
     if st != IDX_OK:
@@ -176,6 +202,13 @@ def case_to_device(case, device="cuda", out_row_stride=None, out_bf16=False):
         return torch.from_numpy(np.require(a, requirements=["C", "W"])).to(device)
     t = dict(q=dev(case.q), k=dev(case.k), w=dev(case.w), ks=dev(case.ks), ke=dev(case.ke),
              q_sf=dev(case.q_sf), k_sf=dev(case.k_sf), k_scales=dev(case.k_tok))
+    if getattr(case, "page_size", 0):
+        from . import synth
+        pl = synth.paged_layout(case, case.page_size, seed=7)
+        t.update(k=dev(pl["k_cache"]), k_sf=dev(pl["k_sf_cache"]),
+                 k_scales=dev(pl["k_scales_cache"]), block_table=dev(pl["block_table"]),
+                 page_size=case.page_size, num_pages=pl["num_pages"],
+                 table_stride=pl["table_stride"])
     stride = out_row_stride or case.N
     t["out"] = torch.empty((case.B, case.S, stride),
                            dtype=torch.bfloat16 if out_bf16 else torch.float32, device=device)
@@ -186,8 +219,15 @@ def case_to_device(case, device="cuda", out_row_stride=None, out_bf16=False):
 
 
 def run_case(case, t, stream=None, clean=None):
-    """indexer_logits on tensors made by case_to_device."""
-    indexer_logits(t["q"], t["q_sf"], t["k"], t["k_sf"], t["k_scales"], t["w"], t["ks"],
-                   t["ke"], case.sm_scale, case.clean if clean is None else clean, t["out"],
-                   t["shape"], stream)
+    """indexer_logits (indexer_paged_logits for a paged case) on tensors made
+    by case_to_device."""
+    clean = case.clean if clean is None else clean
+    if "block_table" in t:
+        indexer_paged_logits(t["q"], t["q_sf"], t["k"], t["k_sf"], t["k_scales"], t["w"],
+                             t["ks"], t["ke"], case.sm_scale, clean, t["out"], t["shape"],
+                             t["block_table"], t["page_size"], t["num_pages"],
+                             t["table_stride"], stream)
+    else:
+        indexer_logits(t["q"], t["q_sf"], t["k"], t["k_sf"], t["k_scales"], t["w"], t["ks"],
+                       t["ke"], case.sm_scale, clean, t["out"], t["shape"], stream)
     return t["out"]

@@ -26,7 +26,7 @@ struct DeviceInfo {
   bool valid = false;
   int sm_count = 0;
   int cc_major = 0, cc_minor = 0;
-  bool smem_set[16] = {};  // per kernel instantiation (format, sign, output type)
+  bool smem_set[32] = {};  // per kernel instantiation (format, sign, output type, paging)
   bool plan_attr_set = false;
 };
 
@@ -160,11 +160,12 @@ int encode_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, in
   return r == CUDA_SUCCESS ? IDX_OK : IDX_ERR_CUDA;
 }
 
-template <int FMT, bool NEG_EPI, bool OUT_BF16>
+template <int FMT, bool NEG_EPI, bool OUT_BF16, bool PAGED>
 int launch_kernel(const KernelParams& prm, int grid, DeviceInfo* di, cudaStream_t stream) {
   constexpr int smem = dsa::Layout<FMT>::kBytes;
-  auto kern = dsa::indexer_logits_kernel<FMT, NEG_EPI, OUT_BF16>;
-  bool& attr_set = di->smem_set[FMT * 4 + (NEG_EPI ? 2 : 0) + (OUT_BF16 ? 1 : 0)];
+  auto kern = dsa::indexer_logits_kernel<FMT, NEG_EPI, OUT_BF16, PAGED>;
+  bool& attr_set =
+      di->smem_set[FMT * 8 + (NEG_EPI ? 4 : 0) + (OUT_BF16 ? 2 : 0) + (PAGED ? 1 : 0)];
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
@@ -177,8 +178,11 @@ int launch_kernel(const KernelParams& prm, int grid, DeviceInfo* di, cudaStream_
 
 template <int FMT, bool NEG_EPI>
 int launch(const KernelParams& prm, int grid, DeviceInfo* di, cudaStream_t stream) {
-  return prm.out_bf16 ? launch_kernel<FMT, NEG_EPI, true>(prm, grid, di, stream)
-                      : launch_kernel<FMT, NEG_EPI, false>(prm, grid, di, stream);
+  if (prm.block_table != nullptr)
+    return prm.out_bf16 ? launch_kernel<FMT, NEG_EPI, true, true>(prm, grid, di, stream)
+                        : launch_kernel<FMT, NEG_EPI, false, true>(prm, grid, di, stream);
+  return prm.out_bf16 ? launch_kernel<FMT, NEG_EPI, true, false>(prm, grid, di, stream)
+                      : launch_kernel<FMT, NEG_EPI, false, false>(prm, grid, di, stream);
 }
 
 }  // namespace
@@ -222,14 +226,25 @@ int64_t indexer_set_wait_limit_ns(int64_t ns) {
 namespace {
 
 // Validate, build the tensor maps and launch one call. `fixed_scratch` is
-// null for indexer_logits (scratch per (device, stream), allocated on first
-// use) or selects the no-allocation variant's fixed device array.
+// false for indexer_logits (scratch per (device, stream), allocated on first
+// use) or selects the no-allocation variant's fixed device array. `paged` is
+// null for contiguous keys.
 int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint8_t* k_sf,
                    const float* k_scales, const void* w, const int32_t* ks, const int32_t* ke,
                    float sm_scale, int clean, void* out, const idx_shape* shape,
-                   cudaStream_t stream, bool fixed_scratch) {
+                   cudaStream_t stream, bool fixed_scratch, const idx_paged* paged = nullptr) {
   if (!shape || !q || !k || !w || !ks || !ke || !out) return IDX_ERR_NULL;
   const idx_shape sh = *shape;
+  idx_paged pg{};
+  if (paged) {
+    pg = *paged;
+    if (!pg.block_table) return IDX_ERR_NULL;
+    if (pg.page_size < 64 || pg.page_size % 64 != 0 || pg.num_pages < 1 || pg.reserved != 0 ||
+        sh.k_batch_bytes != 0 || sh.N < 1 ||
+        pg.table_stride < (static_cast<int64_t>(sh.N) + pg.page_size - 1) / pg.page_size ||
+        static_cast<int64_t>(pg.num_pages) * pg.page_size >= (int64_t(1) << 31))
+      return IDX_ERR_SHAPE;
+  }
   if (sh.fmt < IDX_FMT_BF16 || sh.fmt > IDX_FMT_MXFP4) return IDX_ERR_FORMAT;
   if (sh.w_fmt != IDX_W_F32 && sh.w_fmt != IDX_W_BF16) return IDX_ERR_FORMAT;
   const bool mx = sh.fmt == IDX_FMT_MXFP8 || sh.fmt == IDX_FMT_MXFP4;
@@ -297,10 +312,24 @@ int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
     if ((st = encode_map(&prm.tmap_q, q, dt, 2, dims, strides, box, swz))) return st;
   }
   {
-    const uint64_t dims[3] = {row_elems, static_cast<uint64_t>(sh.N), static_cast<uint64_t>(sh.B)};
-    const uint64_t strides[2] = {static_cast<uint64_t>(k_row), static_cast<uint64_t>(k_batch)};
-    const uint32_t box[3] = {panel_elems, static_cast<uint32_t>(dsa::kKeysPerTile), 1};
-    if ((st = encode_map(&prm.tmap_k, k, dt, 3, dims, strides, box, swz))) return st;
+    if (!paged) {
+      const uint64_t dims[3] = {row_elems, static_cast<uint64_t>(sh.N),
+                                static_cast<uint64_t>(sh.B)};
+      const uint64_t strides[2] = {static_cast<uint64_t>(k_row), static_cast<uint64_t>(k_batch)};
+      const uint32_t box[3] = {panel_elems, static_cast<uint32_t>(dsa::kKeysPerTile), 1};
+      if ((st = encode_map(&prm.tmap_k, k, dt, 3, dims, strides, box, swz))) return st;
+    } else {
+      // the whole cache as rows of keys; a box is 64 keys inside one page
+      const uint64_t dims[2] = {row_elems,
+                                static_cast<uint64_t>(pg.num_pages) * pg.page_size};
+      const uint64_t strides[1] = {static_cast<uint64_t>(k_row)};
+      const uint32_t box[2] = {panel_elems, 64};
+      if ((st = encode_map(&prm.tmap_k, k, dt, 2, dims, strides, box, swz))) return st;
+      prm.block_table = pg.block_table;
+      prm.page_size = pg.page_size;
+      prm.table_stride = pg.table_stride;
+      prm.num_pages = pg.num_pages;
+    }
   }
   prm.q_sf = q_sf;
   prm.k_sf = k_sf;
@@ -372,6 +401,16 @@ int indexer_logits_noalloc(const void* q, const uint8_t* q_sf, const void* k,
   if (kScratchWordsPerCall > kFixedScratchWords) return IDX_ERR_SCRATCH;
   return enqueue_logits(q, q_sf, k, k_sf, k_scales, w, ks, ke, sm_scale, clean, out, shape,
                         reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+int indexer_paged_logits(const void* q, const uint8_t* q_sf, const void* k_cache,
+                         const uint8_t* k_sf_cache, const float* k_scales_cache, const void* w,
+                         const int32_t* ks, const int32_t* ke, float sm_scale, int clean,
+                         void* out, const idx_shape* shape, const idx_paged* paged,
+                         idx_stream_t stream) {
+  if (!paged) return IDX_ERR_NULL;
+  return enqueue_logits(q, q_sf, k_cache, k_sf_cache, k_scales_cache, w, ks, ke, sm_scale, clean,
+                        out, shape, reinterpret_cast<cudaStream_t>(stream), false, paged);
 }
 
 int indexer_get_last_error(idx_stream_t stream_) {

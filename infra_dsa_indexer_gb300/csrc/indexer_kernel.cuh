@@ -87,7 +87,7 @@ struct UnitInfo {
 
 struct KernelParams {
   CUtensorMap tmap_q;  // [B*S*H rows, D] view of Q
-  CUtensorMap tmap_k;  // [B, N, D] view of K
+  CUtensorMap tmap_k;  // [B, N, D] view of K, or [pages * page_size, D] of a paged cache
   const uint8_t* q_sf;
   const uint8_t* k_sf;
   const float* k_scales;
@@ -95,6 +95,13 @@ struct KernelParams {
   const int32_t* ks;
   const int32_t* ke;
   const int32_t* perm;  // [B,S] row order within each batch, or null (identity)
+  // Paged keys (null: contiguous [B, N] keys): key j of batch b is row
+  // j % page_size of page block_table[b * table_stride + j / page_size] of
+  // the cache; key scales (k_sf, k_scales) follow the same rows.
+  const int32_t* block_table;
+  int32_t page_size;     // multiple of 64
+  int32_t table_stride;
+  int32_t num_pages;     // page numbers are clamped to [0, num_pages)
   void* out;         // FP32, or BF16 when out_bf16
   int32_t* scratch;  // [0] unit counter, [1] finished CTAs, [2] error word
   int64_t out_row_stride;
@@ -207,6 +214,17 @@ __device__ __forceinline__ int clampi(int v, int lo, int hi) {
   return v < lo ? lo : (v > hi ? hi : v);
 }
 
+// Cache row of key j (0 <= j < N) of batch b: j itself past the batch's
+// first key for contiguous keys, else through the page table.
+template <bool PAGED>
+__device__ __forceinline__ int64_t key_row(const KernelParams& p, int b, int j) {
+  if constexpr (!PAGED) return static_cast<int64_t>(b) * p.N + j;
+  const int page = clampi(
+      __ldg(p.block_table + static_cast<int64_t>(b) * p.table_stride + j / p.page_size), 0,
+      p.num_pages - 1);
+  return static_cast<int64_t>(page) * p.page_size + j % p.page_size;
+}
+
 __device__ __forceinline__ void raise_error(int32_t* scratch, volatile int* abort_flag, int code) {
   *abort_flag = 1;
   atomicExch(scratch + 2, code);
@@ -298,7 +316,8 @@ __device__ __forceinline__ void mma_step(uint32_t d_tmem, uint64_t a_desc, uint6
 // NEG_EPI: the epilogue applies a negative sm_scale itself (MXFP4, whose MMA
 // kind has no negate bit); every other case negates the MMA's A operand.
 // OUT_BF16: the logits are stored as BF16 (round to nearest even).
-template <int FMT, bool NEG_EPI, bool OUT_BF16>
+// PAGED: the keys (and key scales) are read through the page table.
+template <int FMT, bool NEG_EPI, bool OUT_BF16, bool PAGED>
 __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
     indexer_logits_kernel(const __grid_constant__ KernelParams p) {
   using T = Traits<FMT>;
@@ -532,18 +551,33 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         if (lane == 0) {
           mbar_arrive_expect_tx(&k_full[st], L::kKTileBytes);
           uint8_t* kdst = kbuf + st * L::kKTileBytes;
+          if constexpr (!PAGED) {
 #pragma unroll
-          for (int pnl = 0; pnl < L::kPanels; ++pnl)
-            tma_load_3d(kdst + pnl * L::kKPanelBytes, &p.tmap_k, &k_full[st],
-                        pnl * (T::kSwizzleBytes / T::kTmaElemBytes), t * kKeysPerTile, b, pol_k);
+            for (int pnl = 0; pnl < L::kPanels; ++pnl)
+              tma_load_3d(kdst + pnl * L::kKPanelBytes, &p.tmap_k, &k_full[st],
+                          pnl * (T::kSwizzleBytes / T::kTmaElemBytes), t * kKeysPerTile, b, pol_k);
+          } else {
+            // Paged: two 64-key boxes, each inside one page (page_size is a
+            // multiple of 64). A box wholly past N loads the page of key 0
+            // (rows no window reads) so that no table entry past the
+            // batch's keys is used.
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int k0 = t * kKeysPerTile + 64 * h;
+              const int prow = static_cast<int>(key_row<PAGED>(p, b, k0 < p.N ? k0 : 0));
+#pragma unroll
+              for (int pnl = 0; pnl < L::kPanels; ++pnl)
+                tma_load_2d(kdst + pnl * L::kKPanelBytes + h * 64 * T::kSwizzleBytes, &p.tmap_k,
+                            &k_full[st], pnl * (T::kSwizzleBytes / T::kTmaElemBytes), prow, pol_k);
+            }
+          }
         }
         if constexpr (T::kMX) {
           uint8_t* dst = sfa_s + st * kSfaBytes + 16 * lane;
-          const uint8_t* src = p.k_sf + (static_cast<int64_t>(b) * p.N + t * kKeysPerTile) * 4;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const int m = 32 * c + lane;
-            if (t * kKeysPerTile + m < p.N) cp_async_4(dst + 4 * c, src + 4 * m);
+            const int j = t * kKeysPerTile + 32 * c + lane;
+            if (j < p.N) cp_async_4(dst + 4 * c, p.k_sf + key_row<PAGED>(p, b, j) * 4);
           }
           cp_async_arrive(&sf_full[st]);
         }
@@ -697,10 +731,10 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       // Per-key scale (E4M3), loaded one tile ahead so that its latency
       // overlaps the previous tile instead of stalling the loop head.
       const bool key_scaled = FMT == kFmtE4M3 && p.k_scales != nullptr;
-      const float* kscale_b = key_scaled ? p.k_scales + static_cast<int64_t>(b) * p.N : nullptr;
       auto load_kscale = [&](int t) {
         const int jj = t * kKeysPerTile + quarter * 32 + lane;
-        return (key_scaled && t < c1 && jj < p.N) ? __ldg(kscale_b + jj) : 1.f;
+        return (key_scaled && t < c1 && jj < p.N) ? __ldg(p.k_scales + key_row<PAGED>(p, b, jj))
+                                                   : 1.f;
       };
       float kscale_next = load_kscale(c0);
       bool ok = true;

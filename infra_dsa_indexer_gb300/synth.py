@@ -55,6 +55,7 @@ class Case:
     k_tok: np.ndarray | None = None  # [B,N] float32 per-token K scale
     clean: bool = True
     group_rows: bool = False      # windows are irregular: ask the call to group rows
+    page_size: int = 0            # > 0: the keys go to the GPU through a paged cache
 
     def in_window_pairs(self) -> int:
         lo = np.clip(self.ks.astype(np.int64), 0, self.N)
@@ -153,6 +154,59 @@ def irregular_windows(rng, B, S, N, forced_empty=FORCED_EMPTY_ROWS):
     return ks.astype(np.int32), (ks + ln).astype(np.int32)
 
 
+def decode_windows(rng, B, S, N, min_context):
+    """Decode: batch b has a context of ctx_b ~ U[min_context, N] keys and S
+    new query tokens at its end; token t sees [0, ctx_b - S + t + 1)."""
+    ctx = rng.integers(min_context, N + 1, size=B, dtype=np.int64)
+    t = np.arange(S, dtype=np.int64)
+    ke = np.clip(ctx[:, None] - S + t[None, :] + 1, 0, N)
+    return np.zeros((B, S), dtype=np.int32), ke.astype(np.int32)
+
+
+def paged_layout(case, page_size, seed=0, spare_pages=3):
+    """Scatter the case's keys (and key scales) into a page cache: batch b's
+    pages get distinct page numbers in a random order, with `spare_pages`
+    pages no key maps to; rows past N in the last page of a batch and the
+    spare pages hold random bytes (no window reads them). Returns a dict with
+    k_cache and k_sf_cache as bytes [num_pages, page_size, bytes per key]
+    (k_sf_cache None for plain formats), k_scales_cache FP32 [num_pages,
+    page_size] or None, block_table [B, stride] int32, num_pages and
+    table_stride."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    B, N = case.B, case.N
+    per = -(-N // page_size)
+    num_pages = B * per + spare_pages
+    order = rng.permutation(num_pages)[: B * per].reshape(B, per).astype(np.int32)
+    stride = per + 1
+    table = np.full((B, stride), -5, dtype=np.int32)       # one entry past the keys, never read
+    table[:, :per] = order
+
+    def scatter(src):
+        """[B, N, ...] array -> random-filled byte cache [num_pages, page_size, bytes]."""
+        if src is None:
+            return None
+        sb = np.ascontiguousarray(src).view(np.uint8).reshape(B, N, -1)
+        cache = rng.integers(0, 256, size=(num_pages, page_size, sb.shape[-1]), dtype=np.uint8)
+        for b in range(B):
+            for i in range(per):
+                n = min(page_size, N - i * page_size)
+                cache[order[b, i], :n] = sb[b, i * page_size: i * page_size + n]
+        return cache
+
+    k_cache = scatter(case.k)
+    k_sf_cache = scatter(case.k_sf)
+    k_scales_cache = None
+    if case.k_tok is not None:
+        # random bytes could be NaN scales: spare rows get 1.0 instead
+        k_scales_cache = np.ones((num_pages, page_size), dtype=np.float32)
+        for b in range(B):
+            for i in range(per):
+                n = min(page_size, N - i * page_size)
+                k_scales_cache[order[b, i], :n] = case.k_tok[b, i * page_size: i * page_size + n]
+    return dict(k_cache=k_cache, k_sf_cache=k_sf_cache, k_scales_cache=k_scales_cache,
+                block_table=table, num_pages=num_pages, table_stride=stride)
+
+
 def thd_windows(seqlens_q, seqlens_k, causal=True):
     """Windows of sequences packed along the row and key axes of one batch
     (the THD layout: cu_seqlens are the prefix sums of the lengths). Query
@@ -178,13 +232,16 @@ def thd_windows(seqlens_q, seqlens_k, causal=True):
 def make_case(fmt, B, S, N, H=64, D=128, *, seed=0, windows="full",
               w_fmt=W_F32, w_std=1.0 / 8.0, sm_scale=None, ks=None, ke=None,
               zero=False, name=None, mx_unit_scales=False, group_rows=False,
-              thd=None) -> Case:
+              thd=None, page_size=0, min_context=1) -> Case:
     """Draw Q, K ~ N(0,1), W ~ N(0, w_std^2), quantise to `fmt`.
 
     windows: "full" ([0,N)), "causal" ([0, N-S+i+1)), "causal_excl"
     ([0, N-S+i)), "irregular" (random, see irregular_windows), "thd" (packed
     sequences, thd = (seqlens_q, seqlens_k) summing to S and N; see
-    thd_windows), or give ks/ke.
+    thd_windows), "decode" (S new tokens at the end of a context of
+    U[min_context, N] keys per batch; see decode_windows), or give ks/ke.
+    page_size > 0 marks the case for the paged-key entry point (see
+    paged_layout); the logical keys stay in `k`.
     zero=True makes all-zero Q/K/W (MX scales = 1), as in the pages' timing
     workload."""
     rng = np.random.Generator(np.random.PCG64(seed))
@@ -235,6 +292,8 @@ def make_case(fmt, B, S, N, H=64, D=128, *, seed=0, windows="full",
             ks, ke = causal_windows(B, S, N, N - S)
         elif windows == "irregular":
             ks, ke = irregular_windows(rng, B, S, N)
+        elif windows == "decode":
+            ks, ke = decode_windows(rng, B, S, N, min_context)
         elif windows == "thd":
             lq, lk = thd
             if B != 1 or sum(lq) != S or sum(lk) != N:
@@ -247,7 +306,7 @@ def make_case(fmt, B, S, N, H=64, D=128, *, seed=0, windows="full",
     return Case(name=name or f"{FMT_NAMES[fmt]}_B{B}_S{S}_N{N}", fmt=fmt, B=B,
                 S=S, N=N, H=H, D=D, sm_scale=sm_scale, q=q, k=k, w=w,
                 w_fmt=w_fmt, ks=ks, ke=ke, q_sf=q_sf, k_sf=k_sf, k_tok=k_tok,
-                group_rows=group_rows)
+                group_rows=group_rows, page_size=page_size)
 
 
 # The five workloads, by what they are. Seed = position in this list.
@@ -276,6 +335,10 @@ WORKLOADS = {
     "thd_bf16_3seq_8192x32768": dict(fmt=FMT_BF16, B=1, S=8192, N=32768, windows="thd",
                                      thd=((4096, 2560, 1536), (16384, 10240, 6144)),
                                      w_fmt=W_F32, seed=8),
+    # Decode: 64 sequences, 2 new tokens each, contexts U[16384, 32768], keys
+    # E4M3 with per-key scales in a cache of 64-key pages in random order.
+    "paged_fp8_decode_64x2_32768": dict(fmt=FMT_E4M3, B=64, S=2, N=32768, windows="decode",
+                                        min_context=16384, page_size=64, w_fmt=W_F32, seed=9),
 }
 
 

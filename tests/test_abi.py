@@ -116,3 +116,35 @@ def test_binding_raises_without_cuda_tensors(lib):
     t = torch.zeros(4)
     with pytest.raises(ValueError):
         binding.indexer_logits(t, None, t, None, None, t, t, t, 1.0, True, t, shp())
+
+
+def paged_call(lib, shape, paged, **over):
+    args = dict(q=FAKE, q_sf=None, k=FAKE, k_sf=None, k_scales=None, w=FAKE, ks=FAKE, ke=FAKE,
+                sm_scale=ctypes.c_float(0.1), clean=1, out=FAKE)
+    args.update(over)
+    return lib.indexer_paged_logits(args["q"], args["q_sf"], args["k"], args["k_sf"],
+                                    args["k_scales"], args["w"], args["ks"], args["ke"],
+                                    args["sm_scale"], args["clean"], args["out"],
+                                    ctypes.byref(shape),
+                                    ctypes.byref(paged) if paged is not None else None, None)
+
+
+@pytest.mark.parametrize("paged_kw,shape_kw,status", [
+    (None, {}, 1),                                            # no descriptor
+    (dict(block_table=None), {}, 1),
+    (dict(page_size=32), {}, 2),                              # not a multiple of 64
+    (dict(page_size=0), {}, 2),
+    (dict(table_stride=1), dict(N=100), 2),                   # needs ceil(100 / 64) = 2
+    (dict(num_pages=0), {}, 2),
+    (dict(reserved=1), {}, 2),
+    ({}, dict(k_batch_bytes=4096), 2),                        # no batch stride in a cache
+    (dict(num_pages=1 << 26), {}, 2),                         # rows beyond int32
+])
+def test_paged_host_validation(lib, paged_kw, shape_kw, status):
+    pg = None
+    if paged_kw is not None:
+        base = dict(block_table=0x2000, table_stride=4, page_size=64, num_pages=8, reserved=0)
+        base.update(paged_kw)
+        pg = binding.idx_paged(ctypes.c_void_p(base["block_table"]), base["table_stride"],
+                               base["page_size"], base["num_pages"], base["reserved"])
+    assert paged_call(lib, shp(**shape_kw), pg) == status

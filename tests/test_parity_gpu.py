@@ -235,7 +235,8 @@ def test_thd_packed_sequences(fmt):
                                        ("mxfp8_2048x32768", 256),
                                        ("mxfp4_2048x32768", 256),
                                        ("mxfp4_8192x65536", 1024),
-                                       ("thd_bf16_3seq_8192x32768", 256)])
+                                       ("thd_bf16_3seq_8192x32768", 256),
+                                       ("paged_fp8_decode_64x2_32768", 8)])
 def test_full_size_workload(name, step):
     case = synth.make_workload(name)
     t = binding.case_to_device(case)
