@@ -712,6 +712,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       const int b = in.b, c0 = in.c0, c1 = in.c1, t0 = in.t0, t1 = in.t1, flags = in.flags;
       int lo[R], hi[R];
       char* orow[R];  // null for a row past S (nothing is stored for it)
+      bool any_row = false;
       constexpr bool obf = OUT_BF16;
 #pragma unroll
       for (int r = 0; r < R; ++r) {
@@ -721,6 +722,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         orow[r] = row < 0 ? nullptr
                           : static_cast<char*>(p.out) +
                                 static_cast<int64_t>(row) * p.out_row_stride * (obf ? 2 : 4);
+        any_row |= row >= 0;
       }
       const float* wrows = reinterpret_cast<const float*>(wbuf + slot * L::kWBytes) + r0 * kHeads;
       if (p.clean && (flags & 1)) {
@@ -738,42 +740,59 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       };
       float kscale_next = load_kscale(c0);
       bool ok = true;
-      for (int t = c0; t < c1; ++t, ++aiter) {
-        const int acc = aiter % kAccBufs;
-        const int j = t * kKeysPerTile + quarter * 32 + lane;
-        const float kscale = kscale_next;
-        kscale_next = load_kscale(t + 1);
-        if (!mbar_wait(&acc_full[acc], (aiter / kAccBufs) & 1, abort_flag, p.timeout_ns)) {
-          ok = false;
-          break;
+      if (PAGED && !any_row) {
+        // Every row of this warp is past S (a partial last block; decode with
+        // 1-2 new tokens per sequence): only hand each accumulator back.
+        // Kept to the paged kernels: in the others its mere presence slowed
+        // the E4M3 tile loop, and there the absent rows are just computed
+        // and not stored.
+        for (int t = c0; t < c1; ++t, ++aiter) {
+          if (!mbar_wait(&acc_full[aiter % kAccBufs], (aiter / kAccBufs) & 1, abort_flag,
+                         p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[aiter % kAccBufs]);
         }
-        tc_fence_after();
-        __syncwarp();  // tcgen05.ld is warp-collective: converge first
-        // Read the rows' 64 columns each, hand the accumulator back, reduce.
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                               acc * kBlockN + r0 * kHeads;
-        uint32_t v[R][64];
-        RowAcc<NEG_EPI, T::kReluAllAdd> racc[R];
+      } else {
+        for (int t = c0; t < c1; ++t, ++aiter) {
+          const int acc = aiter % kAccBufs;
+          const int j = t * kKeysPerTile + quarter * 32 + lane;
+          const float kscale = kscale_next;
+          kscale_next = load_kscale(t + 1);
+          if (!mbar_wait(&acc_full[acc], (aiter / kAccBufs) & 1, abort_flag, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          __syncwarp();  // tcgen05.ld is warp-collective: converge first
+          // Read the rows' 64 columns each, hand the accumulator back, reduce.
+          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                 acc * kBlockN + r0 * kHeads;
+          uint32_t v[R][64];
+          RowAcc<NEG_EPI, T::kReluAllAdd> racc[R];
 #pragma unroll
-        for (int r = 0; r < R; ++r) racc[r].zero();
+          for (int r = 0; r < R; ++r) racc[r].zero();
 #pragma unroll
-        for (int r = 0; r < R; ++r) tmem_ld_64cols(taddr + r * kHeads, v[r]);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[acc]);
-        head_steps<0, kHeads / 4>(racc, v, wrows);
-        float sums[R];
+          for (int r = 0; r < R; ++r) tmem_ld_64cols(taddr + r * kHeads, v[r]);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[acc]);
+          head_steps<0, kHeads / 4>(racc, v, wrows);
+          float sums[R];
 #pragma unroll
-        for (int r = 0; r < R; ++r) sums[r] = racc[r].total();
-        if (j < p.N) {
+          for (int r = 0; r < R; ++r) sums[r] = racc[r].total();
+          if (j < p.N) {
 #pragma unroll
-          for (int r = 0; r < R; ++r) {
-            if (orow[r] == nullptr) continue;
-            const float v = (j >= lo[r] && j < hi[r]) ? sums[r] * (sm_abs * kscale) : ninf;
-            if (obf)
-              st_cs_b16(orow[r] + 2 * static_cast<int64_t>(j), f32_to_bf16_rn(v));
-            else
-              __stcs(reinterpret_cast<float*>(orow[r]) + j, v);
+            for (int r = 0; r < R; ++r) {
+              if (orow[r] == nullptr) continue;
+              const float v = (j >= lo[r] && j < hi[r]) ? sums[r] * (sm_abs * kscale) : ninf;
+              if (obf)
+                st_cs_b16(orow[r] + 2 * static_cast<int64_t>(j), f32_to_bf16_rn(v));
+              else
+                __stcs(reinterpret_cast<float*>(orow[r]) + j, v);
+            }
           }
         }
       }
