@@ -574,10 +574,20 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         }
         if constexpr (T::kMX) {
           uint8_t* dst = sfa_s + st * kSfaBytes + 16 * lane;
+          if constexpr (!PAGED) {
+            const uint8_t* src =
+                p.k_sf + (static_cast<int64_t>(b) * p.N + t * kKeysPerTile) * 4;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int j = t * kKeysPerTile + 32 * c + lane;
-            if (j < p.N) cp_async_4(dst + 4 * c, p.k_sf + key_row<PAGED>(p, b, j) * 4);
+            for (int c = 0; c < 4; ++c) {
+              const int m = 32 * c + lane;
+              if (t * kKeysPerTile + m < p.N) cp_async_4(dst + 4 * c, src + 4 * m);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int j = t * kKeysPerTile + 32 * c + lane;
+              if (j < p.N) cp_async_4(dst + 4 * c, p.k_sf + key_row<PAGED>(p, b, j) * 4);
+            }
           }
           cp_async_arrive(&sf_full[st]);
         }
@@ -711,7 +721,11 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       if (in.stop) break;
       const int b = in.b, c0 = in.c0, c1 = in.c1, t0 = in.t0, t1 = in.t1, flags = in.flags;
       int lo[R], hi[R];
-      char* orow[R];  // null for a row past S (nothing is stored for it)
+      // Rows past S (a partial last block) are a suffix of the block. Such a
+      // row aliases the warp's first row, which is stored after it (rows go
+      // in reverse below), so only real values land; a warp with no real
+      // row stores nothing (its bound is 0).
+      char* orow[R];
       bool any_row = false;
       constexpr bool obf = OUT_BF16;
 #pragma unroll
@@ -719,11 +733,12 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         lo[r] = in.lo[r0 + r];
         hi[r] = in.hi[r0 + r];
         const int row = in.row[r0 + r];
-        orow[r] = row < 0 ? nullptr
+        orow[r] = row < 0 ? (r > 0 ? orow[0] : nullptr)
                           : static_cast<char*>(p.out) +
                                 static_cast<int64_t>(row) * p.out_row_stride * (obf ? 2 : 4);
         any_row |= row >= 0;
       }
+      const int store_lim = any_row ? p.N : 0;
       const float* wrows = reinterpret_cast<const float*>(wbuf + slot * L::kWBytes) + r0 * kHeads;
       if (p.clean && (flags & 1)) {
 #pragma unroll
@@ -733,10 +748,13 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       // Per-key scale (E4M3), loaded one tile ahead so that its latency
       // overlaps the previous tile instead of stalling the loop head.
       const bool key_scaled = FMT == kFmtE4M3 && p.k_scales != nullptr;
+      const float* kscale_b =
+          key_scaled && !PAGED ? p.k_scales + static_cast<int64_t>(b) * p.N : nullptr;
       auto load_kscale = [&](int t) {
         const int jj = t * kKeysPerTile + quarter * 32 + lane;
-        return (key_scaled && t < c1 && jj < p.N) ? __ldg(p.k_scales + key_row<PAGED>(p, b, jj))
-                                                   : 1.f;
+        if (!(key_scaled && t < c1 && jj < p.N)) return 1.f;
+        if constexpr (PAGED) return __ldg(p.k_scales + key_row<PAGED>(p, b, jj));
+        return __ldg(kscale_b + jj);
       };
       float kscale_next = load_kscale(c0);
       bool ok = true;
@@ -783,10 +801,9 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
           float sums[R];
 #pragma unroll
           for (int r = 0; r < R; ++r) sums[r] = racc[r].total();
-          if (j < p.N) {
+          if (j < store_lim) {
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-              if (orow[r] == nullptr) continue;
+            for (int r = R - 1; r >= 0; --r) {
               const float v = (j >= lo[r] && j < hi[r]) ? sums[r] * (sm_abs * kscale) : ninf;
               if (obf)
                 st_cs_b16(orow[r] + 2 * static_cast<int64_t>(j), f32_to_bf16_rn(v));
