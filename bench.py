@@ -44,13 +44,15 @@ L2_FLUSH_BYTES = 256 << 20
 # workload, with the digest of the kernel sources it was taken on (see
 # profiles/). Reported as roofline.traffic only while the sources still match.
 PROFILED_TRAFFIC = {
-    "bf16_batched_causal_4096": ("67f0857fb65d0ffb", 137.465088e6 + 79.895552e6),
-    "fp8_per_token_2048x32768": ("67f0857fb65d0ffb", 21.673216e6 + 207.764224e6),
-    "mxfp8_2048x32768": ("67f0857fb65d0ffb", 22.211072e6 + 208.051712e6),
-    "mxfp4_2048x32768": ("67f0857fb65d0ffb", 11.729408e6 + 208.220672e6),
-    "mxfp8_8192x65536": ("67f0857fb65d0ffb", 81478912 + 2087796480),
-    "mxfp4_8192x65536": ("67f0857fb65d0ffb", 43056128 + 2087727872),
-    "mxfp4_irregular_8192x65536": ("67f0857fb65d0ffb", 42290944 + 2086134528),
+    "bf16_batched_causal_4096": ("015898b0b5a96b95", 137.478912e6 + 79.435008e6),
+    "fp8_per_token_2048x32768": ("015898b0b5a96b95", 21.686016e6 + 207.751680e6),
+    "mxfp8_2048x32768": ("015898b0b5a96b95", 22.499328e6 + 207.826176e6),
+    "mxfp4_2048x32768": ("015898b0b5a96b95", 11.749632e6 + 207.739136e6),
+    "paged_fp8_decode_64x2_32768": ("015898b0b5a96b95", 208.231424e6 + 11.180288e6),
+    "mxfp8_8192x65536": ("015898b0b5a96b95", 80266240 + 2088202496),
+    "mxfp4_8192x65536": ("015898b0b5a96b95", 43337216 + 2087812608),
+    "mxfp4_irregular_8192x65536": ("015898b0b5a96b95", 42276608 + 2085944576),
+    "thd_bf16_3seq_8192x32768": ("015898b0b5a96b95", 144876800 + 1012934400),
 }
 
 
