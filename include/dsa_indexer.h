@@ -78,9 +78,10 @@ typedef enum idx_status {
  * group rows with similar windows into the kernel's 4-row blocks. A block
  * computes the union of its rows' 128-key tiles, so on windows with unrelated
  * starts and lengths consecutive rows waste about 2.4x the work; grouped, about
- * 1.03x. Costs one extra launch (a per-batch sort of the rows by window) and
- * B*S*4 bytes of library scratch on the stream; ignored when S > 16384 and by
- * indexer_logits_noalloc. The logits do not depend on it. */
+ * 1.03x. Costs one extra launch (a per-batch counting sort of the rows by
+ * window) and B*S*4 bytes of library scratch on the stream; ignored by
+ * indexer_logits_noalloc. The logits do not depend on it (nor on the order
+ * of rows inside a bin, which may differ between calls). */
 #define IDX_FLAG_GROUP_ROWS 1
 
 /* idx_shape.flags: write the logits as BF16 (round to nearest even of the

@@ -102,22 +102,21 @@ int get_scratch(int dev, cudaStream_t stream, int64_t words, int32_t** out) {
 }
 
 // Rows are regrouped by window (one planning launch before the logits
-// kernel) when the caller asks for it, the call may allocate, and one batch's
-// rows fit the planner's shared memory.
+// kernel) when the caller asks for it and the call may allocate.
 bool groups_rows(const idx_shape& sh, bool fixed_scratch) {
-  return (sh.flags & IDX_FLAG_GROUP_ROWS) != 0 && !fixed_scratch && sh.S <= dsa::kPlanMaxRows;
+  return (sh.flags & IDX_FLAG_GROUP_ROWS) != 0 && !fixed_scratch;
 }
 
 int launch_plan(const int32_t* ks, const int32_t* ke, const idx_shape& sh, int32_t* perm,
                 DeviceInfo* di, cudaStream_t stream) {
-  const int smem = dsa::plan_pow2(sh.S) * static_cast<int>(sizeof(uint64_t));
   if (!di->plan_attr_set) {
     if (cudaFuncSetAttribute(dsa::plan_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             dsa::kPlanMaxRows * static_cast<int>(sizeof(uint64_t))) != cudaSuccess)
+                             dsa::kPlanSmemBytes) != cudaSuccess)
       return IDX_ERR_CUDA;
     di->plan_attr_set = true;
   }
-  dsa::plan_rows_kernel<<<sh.B, dsa::kPlanThreads, smem, stream>>>(ks, ke, sh.S, sh.N, perm);
+  dsa::plan_rows_kernel<<<sh.B, dsa::kPlanThreads, dsa::kPlanSmemBytes, stream>>>(ks, ke, sh.S,
+                                                                                  sh.N, perm);
   return cudaGetLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }
 

@@ -48,7 +48,7 @@ def test_status_strings(lib):
     assert binding.indexer_version() >= 100
     assert binding.indexer_launches_per_call(shp()) == 1
     assert binding.indexer_launches_per_call(shp(flags=1)) == 2
-    assert binding.indexer_launches_per_call(shp(flags=1, S=16388)) == 1
+    assert binding.indexer_launches_per_call(shp(flags=1, S=16388)) == 2   # any S
 
 
 FAKE = ctypes.c_void_p(0x1000)      # never dereferenced: validation fails first

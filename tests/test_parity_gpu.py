@@ -82,6 +82,24 @@ def test_grouped_rows_irregular_windows(fmt):
     assert np.array_equal(plain.view(np.int32), grouped.view(np.int32))
 
 
+def test_grouped_rows_beyond_16k_rows():
+    # the counting sort has no row limit; grouped equals ungrouped bit for bit
+    import dataclasses
+    S, N = 16388, 700
+    case = synth.make_case(synth.FMT_MXFP4, 1, S, N, seed=77, windows="irregular",
+                           group_rows=True)
+    tg = binding.case_to_device(case)
+    tu = binding.case_to_device(dataclasses.replace(case, group_rows=False))
+    binding.run_case(case, tg)
+    binding.run_case(case, tu)
+    torch.cuda.synchronize()
+    assert binding.indexer_get_last_error() == binding.IDX_OK
+    assert torch.equal(tg["out"].view(torch.int32), tu["out"].view(torch.int32))
+    rows = np.arange(0, S, 97)
+    ref, den = oracle_rows(case, rows=rows)
+    compare(tg["out"].view(-1, N)[torch.from_numpy(rows).cuda()].cpu().numpy(), ref, den)
+
+
 def test_grouped_scratch_grows_across_calls():
     """Grouped calls of growing size on one stream re-size the library's
     scratch; every result stays right, and so does an ungrouped call after."""
