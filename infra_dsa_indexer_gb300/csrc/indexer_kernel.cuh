@@ -11,8 +11,10 @@
 // sections "What" and "Precision / determinism").
 //
 // Work decomposition (own design; the pages' kernels are prior art):
-//  * row-block = 4 consecutive query rows of one batch = 4 x 64 heads = 256
-//    (row, head) pairs; key tile = 128 keys.
+//  * row-block = 4 query rows of one batch (consecutive, or consecutive in
+//    the row planner's order; the last block of a batch may have fewer) =
+//    4 x 64 heads = 256 (row, head) pairs; key tile = 128 keys, contiguous
+//    per batch or read through a page table (PAGED).
 //  * One tcgen05 MMA group per (row-block, key tile) with swapped operands:
 //    A = key tile (M = 128 keys), B = the row-block's Q (N = 256 (row,head)),
 //    K = D = 128. The FP32 accumulator lands in TMEM with one key per lane and
@@ -26,7 +28,8 @@
 //    windows the highest row index), so the persistent grid balances itself.
 //
 // Roles (one CTA per SM; 4 role warps + 8 or 16 epilogue warps):
-//  warp 0       K-tile TMA producer (lane 0); for MX formats all 32 lanes also
+//  warp 0       K-tile TMA producer (lane 0; paged keys: two 64-key boxes per
+//               tile, each inside one page); for MX formats all 32 lanes also
 //               copy the tile's key scale factors into shared memory in the
 //               transposed order the TMEM copy wants (4-byte cp.async each)
 //  warp 1       TMEM allocator + MMA issuer (one lane)
@@ -40,7 +43,7 @@
 //               sub-partition it may access) of rows R*((w-4)/4) .. +R-1; it
 //               loads its rows' accumulator columns, hands the buffer back to
 //               the MMA warp, then does the ReLU.w head sums, the masked FP32
-//               stores and the -inf fill outside the block's tiles. R = 2
+//               (or BF16) stores and the -inf fill outside the block's tiles. R = 2
 //               (8 warps, 168 registers each) halves the per-tile overhead
 //               (waits, stores, loop) and suits BF16, where the MMA is long,
 //               and the MX formats, whose single accumulator serialises MMA
