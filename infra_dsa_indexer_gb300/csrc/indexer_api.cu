@@ -351,11 +351,11 @@ int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
 
   // Units: every row-block split into nchunk pieces of its key tiles. Long
   // rows get pieces of at most ~64 tiles (load balance across the persistent
-  // grid); small problems get enough pieces for about four per SM.
+  // grid); small problems get enough pieces for about eight per SM.
   const int64_t row_blocks = static_cast<int64_t>(sh.B) * prm.blocks_per_batch;
   const int64_t tiles_max = (sh.N + dsa::kKeysPerTile - 1) / dsa::kKeysPerTile;
   int64_t nchunk = (tiles_max + 63) / 64;
-  const int64_t want = (4 * di->sm_count + row_blocks - 1) / row_blocks;
+  const int64_t want = (8 * di->sm_count + row_blocks - 1) / row_blocks;
   nchunk = std::max<int64_t>(nchunk, std::min<int64_t>(want, tiles_max));
   nchunk = std::max<int64_t>(nchunk, 1);
   const int64_t units = row_blocks * nchunk;

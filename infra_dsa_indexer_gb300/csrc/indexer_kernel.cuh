@@ -749,17 +749,31 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
           if (orow[r] != nullptr) fill_neg_inf(orow[r], 0, t0 * kKeysPerTile, tid128, obf);
       }
       // Per-key scale (E4M3), loaded one tile ahead so that its latency
-      // overlaps the previous tile instead of stalling the loop head.
+      // overlaps the previous tile instead of stalling the loop head. Paged
+      // keys need two dependent loads (page number, then scale): the page
+      // number is loaded two tiles ahead, the scale one tile ahead.
       const bool key_scaled = FMT == kFmtE4M3 && p.k_scales != nullptr;
       const float* kscale_b =
           key_scaled && !PAGED ? p.k_scales + static_cast<int64_t>(b) * p.N : nullptr;
       auto load_kscale = [&](int t) {
         const int jj = t * kKeysPerTile + quarter * 32 + lane;
         if (!(key_scaled && t < c1 && jj < p.N)) return 1.f;
-        if constexpr (PAGED) return __ldg(p.k_scales + key_row<PAGED>(p, b, jj));
         return __ldg(kscale_b + jj);
       };
-      float kscale_next = load_kscale(c0);
+      auto load_page = [&](int t) {  // page of this thread's key in tile t, or -1
+        const int jj = t * kKeysPerTile + quarter * 32 + lane;
+        if (!(key_scaled && t < c1 && jj < p.N)) return -1;
+        return clampi(__ldg(p.block_table + static_cast<int64_t>(b) * p.table_stride +
+                            jj / p.page_size),
+                      0, p.num_pages - 1);
+      };
+      auto scale_in_page = [&](int t, int page) {
+        if (page < 0) return 1.f;
+        const int jj = t * kKeysPerTile + quarter * 32 + lane;
+        return __ldg(p.k_scales + static_cast<int64_t>(page) * p.page_size + jj % p.page_size);
+      };
+      int page_ahead = PAGED ? load_page(c0 + 1) : -1;
+      float kscale_next = PAGED ? scale_in_page(c0, load_page(c0)) : load_kscale(c0);
       bool ok = true;
       if (PAGED && !any_row) {
         // Every row of this warp is past S (a partial last block; decode with
@@ -781,7 +795,12 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
           const int acc = aiter % kAccBufs;
           const int j = t * kKeysPerTile + quarter * 32 + lane;
           const float kscale = kscale_next;
-          kscale_next = load_kscale(t + 1);
+          if constexpr (PAGED) {
+            kscale_next = scale_in_page(t + 1, page_ahead);
+            page_ahead = load_page(t + 2);
+          } else {
+            kscale_next = load_kscale(t + 1);
+          }
           if (!mbar_wait(&acc_full[acc], (aiter / kAccBufs) & 1, abort_flag, p.timeout_ns)) {
             ok = false;
             break;
