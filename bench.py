@@ -79,6 +79,8 @@ def parse_args(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--topk", type=int, default=0,
+                    help="also time indexer_topk (k columns per row) on the call's logits")
     ap.add_argument("--out-bf16", action="store_true",
                     help="write the logits as BF16 (IDX_FLAG_OUT_BF16) instead of FP32")
     return ap.parse_args(argv)
@@ -332,6 +334,27 @@ def run_ours(args, dist):
     ms = dist.max(ms_local, device=f"cuda:{dev}")
     value = dist.world * flops / (ms * 1e-3) / 1e12
 
+    # --- top-k over the logits of the call (its own launches and events)
+    topk = None
+    if args.topk:
+        idx = torch.empty(case.B, case.S, args.topk, dtype=torch.int32, device=f"cuda:{dev}")
+        for _ in range(3):
+            binding.indexer_topk(t["out"], args.topk, idx=idx, n=case.N, stream=stream)
+        torch.cuda.synchronize()
+        k_st = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        k_en = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            k_st[i].record(stream)
+            binding.indexer_topk(t["out"], args.topk, idx=idx, n=case.N, stream=stream)
+            k_en[i].record(stream)
+        torch.cuda.synchronize()
+        k_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(k_st, k_en))
+        k_bytes = t["out"].numel() * t["out"].element_size() + idx.numel() * 4
+        topk = {"k": args.topk, "us_per_call": 1e3 * k_ms, "kernel": "dsa::topk_rows_kernel",
+                "bound": "hbm", "algorithmic_bytes_per_launch": k_bytes,
+                "achieved_gbs": k_bytes / (k_ms * 1e-3) / 1e9, "gpu_launches": args.steps}
+
     # --- end to end through the same call: pinned host inputs in, logits out
     e2e = None
     if not args.no_e2e:
@@ -363,6 +386,9 @@ def run_ours(args, dist):
     if dist.rank != 0:
         return
     peaks, peak_src = load_peaks()
+    if topk is not None:
+        topk["peak_gbs"] = peaks["hbm_gbs"]
+        topk["frac"] = topk["achieved_gbs"] / peaks["hbm_gbs"]
     peak = peaks["bf16_tflops"] * FMT_PEAK_RATIO[case.fmt]
     achieved = flops / (ms_local * 1e-3) / 1e12
     srt = sorted(per)
@@ -405,7 +431,7 @@ def run_ours(args, dist):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": DTYPES[case.fmt], "data": "synthetic (seeded N(0,1) inputs, quantised)",
         "config": workload_config(case, args),
-        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "topk": topk,
         "gpu_launches": args.steps * launches_per_call,
         "clocks": clk,
     }

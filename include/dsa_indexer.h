@@ -212,6 +212,26 @@ IDX_API int indexer_paged_logits(const void* q, const uint8_t* q_sf, const void*
                                  float sm_scale, int clean, void* out, const idx_shape* shape,
                                  const idx_paged* paged, idx_stream_t stream);
 
+/* Top-k selection over logits (DeepSeek Sparse Attention keeps each query's
+ * top-2048 keys; the pages name it as the indexer's consumer): for every row,
+ * the column indices of its k largest finite values. -inf (outside the row's
+ * window) is never selected; a row with fewer than k finite values gets all
+ * of them and -1 in the rest of its k slots. Indices come out in no
+ * particular order; among values equal to the k-th largest, any subset of
+ * the right size is taken (the choice may differ between calls).
+ *  logits       device, [rows, row_stride] FP32, or BF16 when logits_bf16 is
+ *               non-zero (the output of indexer_logits with either format);
+ *               base aligned to the element size.
+ *  rows, N      rows >= 1 (at most 2^31 - 1), columns N >= 1, N <= row_stride.
+ *  k            1 <= k.
+ *  idx          device, [rows, idx_stride] int32, idx_stride >= k; written in
+ *               columns [0, k) of every row.
+ * Returns IDX_OK once enqueued; IDX_ERR_NULL, IDX_ERR_SHAPE, IDX_ERR_ALIGN,
+ * IDX_ERR_DEVICE, IDX_ERR_CUDA as for indexer_logits. */
+IDX_API int indexer_topk(const void* logits, int logits_bf16, int64_t rows, int32_t N,
+                         int64_t row_stride, int32_t k, int32_t* idx, int64_t idx_stride,
+                         idx_stream_t stream);
+
 /* Human-readable text for an idx_status value (static storage, never NULL). */
 IDX_API const char* indexer_status_string(int status);
 

@@ -78,6 +78,8 @@ def load():
         lib.indexer_paged_logits.restype = i32
         lib.indexer_paged_logits.argtypes = lib.indexer_logits.argtypes[:12] + [
             ctypes.POINTER(idx_paged), vp]
+        lib.indexer_topk.restype = i32
+        lib.indexer_topk.argtypes = [vp, i32, i64, i32, i64, i32, vp, i64, vp]
         lib.indexer_selftest_wait_timeout.restype = i32
         lib.indexer_selftest_wait_timeout.argtypes = [i64, vp]
         lib.indexer_launches_per_call.restype = i32
@@ -167,6 +169,34 @@ def indexer_paged_logits(q, q_sf, k_cache, k_sf_cache, k_scales_cache, w, ks, ke
                                   ctypes.byref(shape), ctypes.byref(pg), _stream(stream))
     if st != IDX_OK:
         raise IndexerError(st, "indexer_paged_logits")
+
+
+def indexer_topk(logits, k: int, idx=None, n=None, stream=None):
+    """Top-k column indices of every row of a CUDA logits tensor (float32 or
+    bfloat16, last dimension the columns, rows contiguous at a fixed stride):
+    returns (or fills) an int32 tensor [..., k]; -1 pads rows with fewer than
+    k finite values. `n` limits the columns (default: the last dimension)."""
+    if logits.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("logits must be float32 or bfloat16")
+    flat = logits.reshape(-1, logits.shape[-1]) if logits.is_contiguous() else None
+    if flat is None:
+        if logits.dim() < 2 or logits.stride(-1) != 1:
+            raise ValueError("logits rows must be contiguous")
+        flat = logits.view(-1, logits.shape[-1]) if logits.dim() == 2 else None
+        if flat is None:
+            raise ValueError("logits must be 2-D or contiguous")
+    rows, cols = flat.shape
+    stride = flat.stride(0)
+    n = cols if n is None else int(n)
+    if idx is None:
+        idx = torch.empty(logits.shape[:-1] + (k,), dtype=torch.int32, device=logits.device)
+    idx_flat = idx.view(-1, idx.shape[-1])
+    st = load().indexer_topk(_ptr(flat), int(logits.dtype == torch.bfloat16), int(rows), int(n),
+                             int(stride), int(k), _ptr(idx_flat), int(idx_flat.stride(0)),
+                             _stream(stream))
+    if st != IDX_OK:
+        raise IndexerError(st, "indexer_topk")
+    return idx
 
 
 def indexer_selftest_wait_timeout(limit_ns: int, stream=None) -> None:

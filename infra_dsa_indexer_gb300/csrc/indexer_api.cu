@@ -15,6 +15,7 @@
 #include "dsa_indexer.h"
 #include "indexer_kernel.cuh"
 #include "plan_kernel.cuh"
+#include "topk_kernel.cuh"
 
 namespace {
 
@@ -434,6 +435,35 @@ int indexer_get_last_error(idx_stream_t stream_) {
       return IDX_ERR_CUDA;
   }
   return word == 0 ? IDX_OK : (word == dsa::kErrTimeout ? IDX_ERR_TIMEOUT : word);
+}
+
+int indexer_topk(const void* logits, int logits_bf16, int64_t rows, int32_t N,
+                 int64_t row_stride, int32_t k, int32_t* idx, int64_t idx_stride,
+                 idx_stream_t stream_) {
+  if (!logits || !idx) return IDX_ERR_NULL;
+  if (rows < 1 || rows > 0x7fffffffLL || N < 1 || k < 1 || row_stride < N || idx_stride < k)
+    return IDX_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(logits) & (logits_bf16 ? 1u : 3u)) ||
+      (reinterpret_cast<uintptr_t>(idx) & 3u))
+    return IDX_ERR_ALIGN;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return IDX_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo* di = nullptr;
+    int st = get_device_info(dev, &di);
+    if (st) return st;
+    if (di->cc_major != 10 || di->cc_minor != 3) return IDX_ERR_DEVICE;
+  }
+  const dim3 grid(static_cast<unsigned>(rows));
+  if (logits_bf16)
+    dsa::topk_rows_kernel<true><<<grid, dsa::kTopkThreads, 0, stream>>>(logits, row_stride, N, k,
+                                                                        idx, idx_stride);
+  else
+    dsa::topk_rows_kernel<false><<<grid, dsa::kTopkThreads, 0, stream>>>(logits, row_stride, N,
+                                                                         k, idx, idx_stride);
+  return cudaGetLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }
 
 int indexer_selftest_wait_timeout(int64_t limit_ns, idx_stream_t stream_) {

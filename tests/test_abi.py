@@ -148,3 +148,22 @@ def test_paged_host_validation(lib, paged_kw, shape_kw, status):
         pg = binding.idx_paged(ctypes.c_void_p(base["block_table"]), base["table_stride"],
                                base["page_size"], base["num_pages"], base["reserved"])
     assert paged_call(lib, shp(**shape_kw), pg) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(logits=None), 1),
+    (dict(idx=None), 1),
+    (dict(rows=0), 2),
+    (dict(N=0), 2),
+    (dict(k=0), 2),
+    (dict(row_stride=50), 2),                              # < N
+    (dict(idx_stride=3), 2),                               # < k
+    (dict(logits=ctypes.c_void_p(0x1002)), 4),             # FP32 not 4-byte aligned
+    (dict(logits=ctypes.c_void_p(0x1001), bf16=1), 4),     # BF16 not 2-byte aligned
+    (dict(idx=ctypes.c_void_p(0x1002)), 4),
+])
+def test_topk_host_validation(lib, args, status):
+    a = dict(logits=FAKE, bf16=0, rows=4, N=100, row_stride=100, k=8, idx=FAKE, idx_stride=8)
+    a.update(args)
+    assert lib.indexer_topk(a["logits"], a["bf16"], a["rows"], a["N"], a["row_stride"], a["k"],
+                            a["idx"], a["idx_stride"], None) == status
