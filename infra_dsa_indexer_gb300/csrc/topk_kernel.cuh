@@ -5,8 +5,11 @@
 // slots. Indices come out in no particular order; among equal values at the
 // threshold any subset of the right size is taken.
 //
-// One CTA per row, radix select on an order-preserving 32-bit key of the
-// value, 8 bits per digit from the top. Sweep 1 histograms the top digit and
+// One CTA per row. Fast path: a sample of the row in shared memory sets a
+// threshold just below the expected k-th value, one sweep compacts the
+// columns above it (~1.2 k), and the selection finishes in shared memory.
+// Exact path (when the sample misjudges): radix select on an order-preserving
+// 32-bit key of the value, 8 bits per digit from the top. Sweep 1 histograms the top digit and
 // sweep 2 the second one among the elements matching it (per-warp
 // sub-histograms in shared memory); each picks the digit where the count from
 // the top reaches the number still to select. Sweep 3 writes the columns
@@ -23,7 +26,7 @@ namespace dsa {
 
 constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kTopkCand = 3072;  // boundary-bin entries kept in shared memory
+constexpr int kTopkCand = 3840;  // candidate entries kept in shared memory
 
 // Larger value -> larger key; -inf -> 0x007fffff, below every finite value.
 __device__ __forceinline__ uint32_t order_key(uint32_t bits) {
@@ -72,13 +75,15 @@ struct TopkShared {
   uint32_t cand_key[kTopkCand];
   int32_t cand_idx[kTopkCand];
   uint32_t prefix, mask, need, finite, out, ties, ncand;
+  uint32_t kmin, kmax;
 };
 
 // Sum the per-warp histograms, then (warp 0) fix the digit at `shift` where
 // the count from the top reaches sh.need: lane l owns digits 8l .. 8l+7 and a
 // suffix sum over the lanes gives the count above each lane. Records the
 // number of finite candidates in sh.finite when asked. Ends with a barrier.
-__device__ __forceinline__ void topk_pick_digit(TopkShared& sh, int shift, bool count_finite) {
+__device__ __forceinline__ void topk_pick_digit(TopkShared& sh, int shift, bool count_finite,
+                                                uint32_t digit_mask = 255u) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   __syncthreads();
   if (tid < 256) {
@@ -118,7 +123,7 @@ __device__ __forceinline__ void topk_pick_digit(TopkShared& sh, int shift, bool 
         above += c[i];
       }
       sh.prefix = prefix | (static_cast<uint32_t>(d) << shift);
-      sh.mask = mask | (255u << shift);
+      sh.mask = mask | (digit_mask << shift);
       sh.need = need - above;
     }
   }
@@ -130,6 +135,144 @@ __device__ __forceinline__ void topk_clear_hist(TopkShared& sh) {
   __syncthreads();
 }
 
+// Radix select of the sh.need-th largest among keys[0, n) in shared memory
+// (0 marks an empty slot, below every finite key; sh.need must not exceed
+// the non-zero keys): sh.prefix ends as its key, sh.need as the number of
+// keys equal to it still to take. The bits above the highest one where the
+// non-zero keys differ are fixed at once, so the 8-bit digits start where the
+// keys spread (the candidates of a row share their top bits, and a digit
+// they all share would pile every lane's count onto one counter).
+__device__ __forceinline__ void topk_select_in_smem(TopkShared& sh, const uint32_t* keys,
+                                                    uint32_t n) {
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (tid == 0) {
+    sh.kmin = ~0u;
+    sh.kmax = 0u;
+  }
+  __syncthreads();
+  uint32_t mn = ~0u, mx = 0u;
+  for (uint32_t c = tid; c < n; c += kTopkThreads) {
+    const uint32_t key = keys[c];
+    if (key != 0u) {
+      mn = min(mn, key);
+      mx = max(mx, key);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  if ((tid & 31) == 0) {
+    atomicMin(&sh.kmin, mn);
+    atomicMax(&sh.kmax, mx);
+  }
+  __syncthreads();
+  const uint32_t kmin = sh.kmin, kmax = sh.kmax;
+  // highest differing bit p (-1: all equal); bits above p are common
+  const int p = kmin >= kmax ? -1 : 31 - __clz(kmin ^ kmax);
+  const uint32_t common = p < 0 ? ~0u : (p >= 31 ? 0u : ~((2u << p) - 1u));
+  __syncthreads();
+  if (tid == 0) {
+    sh.prefix = kmax & common;
+    sh.mask = common;
+  }
+  int hi = p + 1;  // bits [0, hi) are still free
+  while (hi > 0) {
+    const int shift = hi > 8 ? hi - 8 : 0;
+    const uint32_t width_mask = (1u << (hi - shift)) - 1u;
+    topk_clear_hist(sh);
+    const uint32_t prefix = sh.prefix, mask = sh.mask;
+    for (uint32_t c = tid; c < n; c += kTopkThreads) {
+      const uint32_t key = keys[c];
+      if (key != 0u && (key & mask) == prefix)
+        atomicAdd(&sh.hist[warp][(key >> shift) & width_mask], 1u);
+    }
+    topk_pick_digit(sh, shift, false, width_mask);
+    hi = shift;
+  }
+  __syncthreads();
+}
+
+// Fast path (sample select). Runs of 8 consecutive columns spread over the
+// row (at most kTopkCand keys, in shared memory) give a threshold a little
+// below the expected k-th largest value; one sweep compacts every column at
+// or above it, and the exact selection runs on those in shared memory.
+// Returns false, with nothing written, when the sample misjudged: fewer than
+// k columns reach the threshold although it excluded finite values, or more
+// columns than fit.
+template <bool BF16_IN>
+__device__ bool topk_sample_select(TopkShared& sh, const char* rp, int N, int k, int32_t* out) {
+  const int tid = threadIdx.x;
+  constexpr int kRun = 8;
+  constexpr int kRuns = kTopkCand / kRun;
+  const int step = N >= kRun * kRuns ? (N / kRuns) / kRun * kRun : kRun;
+  if (tid == 0) {
+    sh.ncand = 0;
+    sh.prefix = 0;
+    sh.mask = 0;
+  }
+  __syncthreads();
+  uint32_t nfin_local = 0;
+  for (int s = tid; s < kTopkCand; s += kTopkThreads) {
+    const int j = (s / kRun) * step + s % kRun;
+    const uint32_t key = j < N ? load_key<BF16_IN>(rp, j) : 0u;
+    const bool fin = key > kNegInfKey;
+    sh.cand_key[s] = fin ? key : 0u;  // 0 ranks below every finite key
+    nfin_local += fin ? 1u : 0u;
+  }
+  const int ns = min(N, kRuns * step) / step * kRun + min(kRun, min(N, kRuns * step) % step);
+  atomicAdd(&sh.ncand, nfin_local);
+  __syncthreads();
+  const uint32_t nfin = sh.ncand;
+  // the sample rank expected to have ~1.2 k columns of the row at or above it
+  const uint32_t r = static_cast<uint32_t>(ceilf(1.2f * static_cast<float>(k) *
+                                                 static_cast<float>(ns) / static_cast<float>(N))) + 4u;
+  uint32_t t_est = kNegInfKey + 1u;  // every finite value
+  if (r <= nfin) {
+    if (tid == 0) sh.need = r;
+    topk_select_in_smem(sh, sh.cand_key, kTopkCand);
+    t_est = sh.prefix;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    sh.ncand = 0;
+    sh.prefix = 0;
+    sh.mask = 0;
+    sh.need = static_cast<uint32_t>(k);
+    sh.out = 0;
+    sh.ties = 0;
+  }
+  __syncthreads();
+  for_each_key<BF16_IN>(rp, N, [&](int j, uint32_t key) {
+    if (key < t_est) return;
+    const uint32_t pos = atomicAdd(&sh.ncand, 1u);
+    if (pos < static_cast<uint32_t>(kTopkCand)) {
+      sh.cand_key[pos] = key;
+      sh.cand_idx[pos] = j;
+    }
+  });
+  __syncthreads();
+  const uint32_t nc = sh.ncand;
+  if (nc > static_cast<uint32_t>(kTopkCand)) return false;
+  if (nc < static_cast<uint32_t>(k)) {
+    // right only when the threshold let every finite value through
+    if (t_est != kNegInfKey + 1u) return false;
+    for (uint32_t c = tid; c < nc; c += kTopkThreads) out[c] = sh.cand_idx[c];
+    for (int i = static_cast<int>(nc) + tid; i < k; i += kTopkThreads) out[i] = -1;
+    return true;
+  }
+  topk_select_in_smem(sh, sh.cand_key, nc);
+  const uint32_t thr = sh.prefix, ties = sh.need;
+  for (uint32_t c = tid; c < nc; c += kTopkThreads) {
+    const uint32_t key = sh.cand_key[c];
+    bool t = key > thr;
+    if (key == thr) t = atomicAdd(&sh.ties, 1u) < ties;
+    if (t) out[atomicAdd(&sh.out, 1u)] = sh.cand_idx[c];
+  }
+  return true;
+}
+
 template <bool BF16_IN>
 __global__ void __launch_bounds__(kTopkThreads)
     topk_rows_kernel(const void* __restrict__ logits, int64_t row_stride, int N, int k,
@@ -139,6 +282,10 @@ __global__ void __launch_bounds__(kTopkThreads)
   const int64_t row = blockIdx.x;
   const char* rp = reinterpret_cast<const char*>(logits) + row * row_stride * (BF16_IN ? 2 : 4);
   int32_t* out = idx + row * idx_stride;
+  if (topk_sample_select<BF16_IN>(sh, rp, N, k, out)) return;
+
+  // Exact path: radix select by sweeps over the row.
+  __syncthreads();
   if (tid == 0) {
     sh.prefix = 0;
     sh.mask = 0;
