@@ -37,7 +37,8 @@ def check_topk(vals, sel, k):
         assert set(above.tolist()) <= set(picked.tolist()), f"row {r}: misses a larger value"
 
 
-@pytest.mark.parametrize("N,k", [(1, 1), (100, 7), (5000, 2048), (65536, 2048), (3000, 2999)])
+@pytest.mark.parametrize("N,k", [(1, 1), (100, 7), (100, 150), (5000, 2048), (65536, 2048),
+                                 (3000, 2999)])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_topk_random_rows(N, k, dtype):
     g = torch.Generator(device="cuda").manual_seed(N + k)
