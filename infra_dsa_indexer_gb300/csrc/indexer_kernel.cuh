@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
   } else if (warp == 2) {
     // ---------------------------------------------------------- unit scheduler
     // Lane 0 claims units, writes the unit info and starts the Q TMA; all 32
-    // lanes copy the block's head weights into shared memory as FP32 and, for
+    // lanes then copy the block's head weights into shared memory as FP32 and, for
     // MX formats, its Q scale factors in TMEM-copy order.
     if (lane == 0) prefetch_tmap(&p.tmap_q);
     const uint64_t pol_first = policy_evict_first();  // Q block: read once per unit
@@ -437,6 +437,54 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         const int pos = min(blk * kRowsPerBlock + r, p.S - 1);
         grow[r] = b * p.S + (p.perm != nullptr ? __ldg(p.perm + b * p.S + pos) : pos);
       }
+      // Lane 0 first: the windows, the tile range and (for a unit with
+      // tiles) the Q TMA, its bytes announced on unit_full without arriving,
+      // so the load is in flight while the lanes fetch the weights. The
+      // arrive that publishes the unit comes last.
+      if (lane == 0) {
+        int lo_all = p.N, hi_all = 0;
+#pragma unroll
+        for (int r = 0; r < kRowsPerBlock; ++r) {
+          const bool exists = blk * kRowsPerBlock + r < p.S;
+          const int lo = exists ? clampi(__ldg(p.ks + grow[r]), 0, p.N) : 0;
+          const int hi = exists ? clampi(__ldg(p.ke + grow[r]), 0, p.N) : 0;
+          in.row[r] = exists ? grow[r] : -1;
+          in.lo[r] = lo;
+          in.hi[r] = hi;
+          if (lo < hi) {
+            lo_all = min(lo_all, lo);
+            hi_all = max(hi_all, hi);
+          }
+        }
+        int t0 = 0, t1 = 0;
+        if (lo_all < hi_all) {
+          t0 = lo_all / kKeysPerTile;
+          t1 = (hi_all + kKeysPerTile - 1) / kKeysPerTile;
+        }
+        const int len = (t1 - t0 + p.nchunk - 1) / p.nchunk;
+        const int c0 = min(t1, t0 + chunk * len);
+        const int c1 = min(t1, c0 + len);
+        in.stop = 0;
+        in.b = b;
+        in.c0 = c0;
+        in.c1 = c1;
+        in.t0 = t0;
+        in.t1 = t1;
+        in.flags = (chunk == 0 ? 1 : 0) | (chunk == p.nchunk - 1 ? 2 : 0);
+        if (c1 > c0) {
+          mbar_expect_tx(&unit_full[slot], L::kQBlockBytes);
+          // One 64-head box per row and panel; row r lands at rows 64r.. of
+          // the block (a whole number of swizzle atoms).
+          uint8_t* qdst = qbuf + slot * L::kQBlockBytes;
+#pragma unroll
+          for (int r = 0; r < kRowsPerBlock; ++r)
+#pragma unroll
+            for (int pnl = 0; pnl < L::kPanels; ++pnl)
+              tma_load_2d(qdst + pnl * L::kQPanelBytes + r * kHeads * T::kSwizzleBytes,
+                          &p.tmap_q, &unit_full[slot], pnl * (T::kSwizzleBytes / T::kTmaElemBytes),
+                          grow[r] * kHeads, pol_first);
+        }
+      }
       // head weights of the 4 rows -> FP32 in shared memory, row-major 4 x 64
       float* wdst = reinterpret_cast<float*>(wbuf + slot * L::kWBytes);
       if (p.w_bf16) {
@@ -474,52 +522,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         cp_async_arrive(&unit_full[slot]);
       }
       __syncwarp();
-      if (lane == 0) {
-        int lo_all = p.N, hi_all = 0;
-#pragma unroll
-        for (int r = 0; r < kRowsPerBlock; ++r) {
-          const bool exists = blk * kRowsPerBlock + r < p.S;
-          const int lo = exists ? clampi(__ldg(p.ks + grow[r]), 0, p.N) : 0;
-          const int hi = exists ? clampi(__ldg(p.ke + grow[r]), 0, p.N) : 0;
-          in.row[r] = exists ? grow[r] : -1;
-          in.lo[r] = lo;
-          in.hi[r] = hi;
-          if (lo < hi) {
-            lo_all = min(lo_all, lo);
-            hi_all = max(hi_all, hi);
-          }
-        }
-        int t0 = 0, t1 = 0;
-        if (lo_all < hi_all) {
-          t0 = lo_all / kKeysPerTile;
-          t1 = (hi_all + kKeysPerTile - 1) / kKeysPerTile;
-        }
-        const int len = (t1 - t0 + p.nchunk - 1) / p.nchunk;
-        const int c0 = min(t1, t0 + chunk * len);
-        const int c1 = min(t1, c0 + len);
-        in.stop = 0;
-        in.b = b;
-        in.c0 = c0;
-        in.c1 = c1;
-        in.t0 = t0;
-        in.t1 = t1;
-        in.flags = (chunk == 0 ? 1 : 0) | (chunk == p.nchunk - 1 ? 2 : 0);
-        if (c1 > c0) {
-          mbar_arrive_expect_tx(&unit_full[slot], L::kQBlockBytes);
-          // One 64-head box per row and panel; row r lands at rows 64r.. of
-          // the block (a whole number of swizzle atoms).
-          uint8_t* qdst = qbuf + slot * L::kQBlockBytes;
-#pragma unroll
-          for (int r = 0; r < kRowsPerBlock; ++r)
-#pragma unroll
-            for (int pnl = 0; pnl < L::kPanels; ++pnl)
-              tma_load_2d(qdst + pnl * L::kQPanelBytes + r * kHeads * T::kSwizzleBytes,
-                          &p.tmap_q, &unit_full[slot], pnl * (T::kSwizzleBytes / T::kTmaElemBytes),
-                          grow[r] * kHeads, pol_first);
-        } else {
-          mbar_arrive(&unit_full[slot]);
-        }
-      }
+      if (lane == 0) mbar_arrive(&unit_full[slot]);
       __syncwarp();
     }
   } else if (warp == 0 && (T::kMX || lane == 0)) {
