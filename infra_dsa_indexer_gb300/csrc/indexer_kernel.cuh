@@ -33,10 +33,11 @@
 //               copy the tile's key scale factors into shared memory in the
 //               transposed order the TMEM copy wants (4-byte cp.async each)
 //  warp 1       TMEM allocator + MMA issuer (one lane)
-//  warp 2       unit scheduler: claims the next unit, reads its windows, stages
-//               its head weights in shared memory as FP32 (and, for MX, its Q
-//               scale factors), and starts the TMA of its Q block, one unit
-//               ahead of the MMA
+//  warp 2       unit scheduler: claims units two ahead and prefetches their
+//               windows, head weights and (MX) Q scale factors into
+//               registers; when a slot frees it stages the weights in shared
+//               memory as FP32 (and the Q scale factors) and starts the TMA
+//               of the unit's Q block, one unit ahead of the MMA
 //  warp 3       idle
 //  warps 4..    epilogue, R = 1 or 2 query rows per warp (a per-format
 //               choice): warp w reads TMEM lanes 32*(w%4)..+31 (the
@@ -358,8 +359,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
     }
     *abort_flag = 0;
     for (int s = 0; s < 2; ++s) {
-      // unit_full: the scheduler's arrive (+ one cp.async arrival per lane for MX)
-      mbar_init(&unit_full[s], T::kMX ? 1 + 32 : 1);
+      mbar_init(&unit_full[s], 1);  // the scheduler's arrive (+ the Q TMA bytes)
       mbar_init(&unit_empty[s], 2 + kNumEpiWarps);  // K producer, MMA commit, epilogue warps
     }
     for (int s = 0; s < kAccBufs; ++s) {
@@ -388,69 +388,59 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
     // nothing: the error word says why
   } else if (warp == 2) {
     // ---------------------------------------------------------- unit scheduler
-    // Lane 0 claims units, writes the unit info and starts the Q TMA; all 32
-    // lanes then copy the block's head weights into shared memory as FP32 and, for
-    // MX formats, its Q scale factors in TMEM-copy order.
+    // A unit is claimed and its rows, windows, weights and (MX) Q scale
+    // words are fetched into registers; once its slot is free, lane 0 writes
+    // the unit info and starts the Q TMA and all 32 lanes store the weights
+    // (FP32) and scale words into the slot. Claiming and fetching take
+    // several microseconds (a contended atomic, then dependent global
+    // loads). With grouped rows (one more dependent load, the row order;
+    // many short units) the next unit is claimed as soon as a slot frees
+    // and fetched right after the current one is published, so that work
+    // overlaps the units in flight; otherwise a unit is claimed only once
+    // its slot is free, which keeps the tail of the persistent grid short.
     if (lane == 0) prefetch_tmap(&p.tmap_q);
     const uint64_t pol_first = policy_evict_first();  // Q block: read once per unit
-    for (uint32_t it = 0;; ++it) {
-      const int slot = it & 1;
-      int ok = 1, u = 0;
-      if (lane == 0) {
-        ok = mbar_wait(&unit_empty[slot], ((it >> 1) & 1) ^ 1, abort_flag, p.timeout_ns);
-        if (ok) u = atomicAdd(p.scratch + 0, 1);
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      u = __shfl_sync(0xffffffffu, u, 0);
-      if (!ok) {
-        if (lane == 0) {
-          raise_error(p.scratch, abort_flag, kErrTimeout);
-          // Let the Q loads (and scale copies) of the units still in the
-          // slots land before the CTA exits.
-          for (uint32_t j = it > 2 ? it - 2 : 0; j < it; ++j)
-            mbar_wait_drain(&unit_full[j & 1], (j >> 1) & 1, p.timeout_ns);
-        }
-        break;
-      }
-      UnitInfo& in = info[slot];
-      if (u >= p.num_units) {
-        if (lane == 0) {
-          in.stop = 1;
-          mbar_arrive(&unit_full[slot]);
-        }
-        if constexpr (T::kMX) cp_async_arrive(&unit_full[slot]);
-        break;
-      }
+    struct Prep {
+      int u, chunk, blk, b;
+      int grow[kRowsPerBlock];
+      UnitInfo in;      // lane 0 only: the info the slot gets
+      float4 w[2];      // this lane's part of the block's FP32 head weights
+      uint32_t sf[kBlockN / 32];  // MX: this lane's Q scale words
+    };
+    // grow[i] for a lane-dependent i, without indexing the array at run time
+    // (which would move it to local memory).
+    auto pick = [](const int (&g)[kRowsPerBlock], int i) {
+      return i == 0 ? g[0] : i == 1 ? g[1] : i == 2 ? g[2] : g[3];
+    };
+    // Fetch everything unit u needs, into registers.
+    auto prepare = [&](int u, Prep& q) {
+      q.u = u;
+      if (u >= p.num_units) return;
       // Units in order: row-blocks from the last (longest causal window) to
       // the first, batches interleaved, chunks of one row-block adjacent.
       const int order = u / p.nchunk;
-      const int chunk = u - order * p.nchunk;
-      const int blk = p.blocks_per_batch - 1 - order / p.B;
-      const int b = order % p.B;
-      // The block's rows: positions 4*blk .. 4*blk+3 of the batch's row order.
-      // Positions past S (a partial last block) read the batch's last row in
-      // that order, so every address stays valid; the row gets an empty
-      // window and is never stored.
-      int grow[kRowsPerBlock];
+      q.chunk = u - order * p.nchunk;
+      q.blk = p.blocks_per_batch - 1 - order / p.B;
+      q.b = order % p.B;
+      // The block's rows: positions 4*blk .. 4*blk+3 of the batch's row
+      // order. Positions past S (a partial last block) read the batch's last
+      // row in that order, so every address stays valid; the row gets an
+      // empty window and is never stored.
 #pragma unroll
       for (int r = 0; r < kRowsPerBlock; ++r) {
-        const int pos = min(blk * kRowsPerBlock + r, p.S - 1);
-        grow[r] = b * p.S + (p.perm != nullptr ? __ldg(p.perm + b * p.S + pos) : pos);
+        const int pos = min(q.blk * kRowsPerBlock + r, p.S - 1);
+        q.grow[r] = q.b * p.S + (p.perm != nullptr ? __ldg(p.perm + q.b * p.S + pos) : pos);
       }
-      // Lane 0 first: the windows, the tile range and (for a unit with
-      // tiles) the Q TMA, its bytes announced on unit_full without arriving,
-      // so the load is in flight while the lanes fetch the weights. The
-      // arrive that publishes the unit comes last.
       if (lane == 0) {
         int lo_all = p.N, hi_all = 0;
 #pragma unroll
         for (int r = 0; r < kRowsPerBlock; ++r) {
-          const bool exists = blk * kRowsPerBlock + r < p.S;
-          const int lo = exists ? clampi(__ldg(p.ks + grow[r]), 0, p.N) : 0;
-          const int hi = exists ? clampi(__ldg(p.ke + grow[r]), 0, p.N) : 0;
-          in.row[r] = exists ? grow[r] : -1;
-          in.lo[r] = lo;
-          in.hi[r] = hi;
+          const bool exists = q.blk * kRowsPerBlock + r < p.S;
+          const int lo = exists ? clampi(__ldg(p.ks + q.grow[r]), 0, p.N) : 0;
+          const int hi = exists ? clampi(__ldg(p.ke + q.grow[r]), 0, p.N) : 0;
+          q.in.row[r] = exists ? q.grow[r] : -1;
+          q.in.lo[r] = lo;
+          q.in.hi[r] = hi;
           if (lo < hi) {
             lo_all = min(lo_all, lo);
             hi_all = max(hi_all, hi);
@@ -462,16 +452,82 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
           t1 = (hi_all + kKeysPerTile - 1) / kKeysPerTile;
         }
         const int len = (t1 - t0 + p.nchunk - 1) / p.nchunk;
-        const int c0 = min(t1, t0 + chunk * len);
-        const int c1 = min(t1, c0 + len);
-        in.stop = 0;
-        in.b = b;
-        in.c0 = c0;
-        in.c1 = c1;
-        in.t0 = t0;
-        in.t1 = t1;
-        in.flags = (chunk == 0 ? 1 : 0) | (chunk == p.nchunk - 1 ? 2 : 0);
-        if (c1 > c0) {
+        q.in.stop = 0;
+        q.in.b = q.b;
+        q.in.c0 = min(t1, t0 + q.chunk * len);
+        q.in.c1 = min(t1, q.in.c0 + len);
+        q.in.t0 = t0;
+        q.in.t1 = t1;
+        q.in.flags = (q.chunk == 0 ? 1 : 0) | (q.chunk == p.nchunk - 1 ? 2 : 0);
+      }
+      if (p.w_bf16) {
+        // lane l: 8 weights = 16 bytes, row l/8, heads 8*(l%8)..
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.w) +
+                                static_cast<int64_t>(pick(q.grow, lane >> 3)) * (kHeads / 8) +
+                                (lane & 7));
+        q.w[0] = make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u),
+                             __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u));
+        q.w[1] = make_float4(__uint_as_float(raw.z << 16), __uint_as_float(raw.z & 0xffff0000u),
+                             __uint_as_float(raw.w << 16), __uint_as_float(raw.w & 0xffff0000u));
+      } else {
+        // float4 f = lane + 32i: row f/16, heads 4*(f%16)..
+        const float4* src = reinterpret_cast<const float4*>(p.w);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int f = lane + 32 * i;
+          q.w[i] = __ldg(src + static_cast<int64_t>(pick(q.grow, f >> 4)) * (kHeads / 4) + (f & 15));
+        }
+      }
+      if constexpr (T::kMX) {
+        // (row, head) m = 32c + lane = 64r + h: the word of row grow[r], head
+        // h, with r = c / 2 (lane < 32).
+#pragma unroll
+        for (int c = 0; c < kBlockN / 32; ++c) {
+          const int m = 32 * c + lane;
+          q.sf[c] = __ldg(reinterpret_cast<const uint32_t*>(p.q_sf) +
+                          static_cast<int64_t>(q.grow[c >> 1]) * kHeads + (m & 63));
+        }
+      }
+    };
+    const bool ahead = p.perm != nullptr;
+    int u_next = 0;
+    Prep cur;
+    if (ahead) {
+      if (lane == 0) u_next = atomicAdd(p.scratch + 0, 1);
+      prepare(__shfl_sync(0xffffffffu, u_next, 0), cur);
+    }
+    for (uint32_t it = 0;; ++it) {
+      const int slot = it & 1;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&unit_empty[slot], ((it >> 1) & 1) ^ 1, abort_flag, p.timeout_ns);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) {
+          raise_error(p.scratch, abort_flag, kErrTimeout);
+          // Let the Q loads of the units still in the slots land before the
+          // CTA exits.
+          for (uint32_t j = it > 2 ? it - 2 : 0; j < it; ++j)
+            mbar_wait_drain(&unit_full[j & 1], (j >> 1) & 1, p.timeout_ns);
+        }
+        break;
+      }
+      if (!ahead) {
+        if (lane == 0) u_next = atomicAdd(p.scratch + 0, 1);
+        prepare(__shfl_sync(0xffffffffu, u_next, 0), cur);
+      }
+      UnitInfo& in = info[slot];
+      if (cur.u >= p.num_units) {
+        if (lane == 0) {
+          in.stop = 1;
+          mbar_arrive(&unit_full[slot]);
+        }
+        break;
+      }
+      // The next claim; its result is first needed after this unit is out.
+      if (ahead && lane == 0) u_next = atomicAdd(p.scratch + 0, 1);
+      if (lane == 0) {
+        in = cur.in;
+        if (cur.in.c1 > cur.in.c0) {
           mbar_expect_tx(&unit_full[slot], L::kQBlockBytes);
           // One 64-head box per row and panel; row r lands at rows 64r.. of
           // the block (a whole number of swizzle atoms).
@@ -482,48 +538,32 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
             for (int pnl = 0; pnl < L::kPanels; ++pnl)
               tma_load_2d(qdst + pnl * L::kQPanelBytes + r * kHeads * T::kSwizzleBytes,
                           &p.tmap_q, &unit_full[slot], pnl * (T::kSwizzleBytes / T::kTmaElemBytes),
-                          grow[r] * kHeads, pol_first);
+                          cur.grow[r] * kHeads, pol_first);
         }
       }
-      // head weights of the 4 rows -> FP32 in shared memory, row-major 4 x 64
-      float* wdst = reinterpret_cast<float*>(wbuf + slot * L::kWBytes);
+      // Head weights of the 4 rows as FP32, row-major 4 x 64.
+      float4* wdst = reinterpret_cast<float4*>(wbuf + slot * L::kWBytes);
       if (p.w_bf16) {
-        // lane l: 8 weights = 16 bytes, row l/8, heads 8*(l%8)..
-        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.w) +
-                                static_cast<int64_t>(grow[lane >> 3]) * (kHeads / 8) + (lane & 7));
-        const uint32_t r[4] = {raw.x, raw.y, raw.z, raw.w};
-        reinterpret_cast<float4*>(wdst)[2 * lane] =
-            make_float4(__uint_as_float(r[0] << 16), __uint_as_float(r[0] & 0xffff0000u),
-                        __uint_as_float(r[1] << 16), __uint_as_float(r[1] & 0xffff0000u));
-        reinterpret_cast<float4*>(wdst)[2 * lane + 1] =
-            make_float4(__uint_as_float(r[2] << 16), __uint_as_float(r[2] & 0xffff0000u),
-                        __uint_as_float(r[3] << 16), __uint_as_float(r[3] & 0xffff0000u));
+        wdst[2 * lane] = cur.w[0];
+        wdst[2 * lane + 1] = cur.w[1];
       } else {
-        // float4 f (lane and lane + 32): row f/16, heads 4*(f%16)..
-        const float4* src = reinterpret_cast<const float4*>(p.w);
-#pragma unroll
-        for (int f = lane; f < kRowsPerBlock * kHeads / 4; f += 32)
-          reinterpret_cast<float4*>(wdst)[f] =
-              __ldg(src + static_cast<int64_t>(grow[f >> 4]) * (kHeads / 4) + (f & 15));
+        wdst[lane] = cur.w[0];
+        wdst[lane + 32] = cur.w[1];
       }
       if constexpr (T::kMX) {
         // Q scale word of (row, head) m = 32c + lane goes to TMEM lane m % 32,
         // column m / 32: in shared memory, chunk m / 128 (one TMEM copy
         // each), row m % 32 (16 bytes), word (m % 128) / 32.
-        // (row, head) m = 64r + h reads the word of row grow[r], head h.
         uint8_t* dst = sfb_s + slot * kSfbBytes;
 #pragma unroll
         for (int c = 0; c < kBlockN / 32; ++c) {
           const int m = 32 * c + lane;
-          const uint8_t* src =
-              p.q_sf + (static_cast<int64_t>(grow[m >> 6]) * kHeads + (m & 63)) * 4;
-          cp_async_4(dst + (m >> 7) * 512 + 16 * lane + 4 * (c & 3), src);
+          *reinterpret_cast<uint32_t*>(dst + (m >> 7) * 512 + 16 * lane + 4 * (c & 3)) = cur.sf[c];
         }
-        cp_async_arrive(&unit_full[slot]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&unit_full[slot]);
-      __syncwarp();
+      if (ahead) prepare(__shfl_sync(0xffffffffu, u_next, 0), cur);
     }
   } else if (warp == 0 && (T::kMX || lane == 0)) {
     // ------------------------------------------------------- K-tile producer
@@ -657,8 +697,9 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
           // read by the MMAs of tile t-2 or earlier, which finished before
           // tile t-1's accumulator could be handed back and its MMAs issued.
           // Copies and MMAs of this thread run in issue order. The scale
-          // words were written by cp.async (generic proxy); the TMEM copy
-          // reads them through the async proxy.
+          // words were written by cp.async (key scales) and plain stores (Q
+          // scales), both generic proxy; the TMEM copy reads them through
+          // the async proxy.
           fence_proxy_async_smem();
           sfa = tmem_base + kSfaCol + 4 * (kiter & 1);
           sfb = tmem_base + kSfbCol + 8 * (units_mma & 1);
