@@ -21,6 +21,7 @@
 // after the first it comes from L2.
 #pragma once
 #include <cstdint>
+#include <type_traits>
 
 namespace dsa {
 
@@ -46,26 +47,38 @@ __device__ __forceinline__ uint32_t load_key(const void* row, int j) {
 
 // Visits every column j < N of the row with f(j, key); four keys per load
 // when the row start is 16-byte aligned (FP32) or 8-byte aligned (BF16).
+// The loads of kUnroll consecutive strides are issued before any key is
+// visited, so each CTA keeps 32 KB of its row in flight.
 template <bool BF16_IN, typename F>
 __device__ __forceinline__ void for_each_key(const char* rp, int N, F&& f) {
   const int tid = threadIdx.x;
   const bool vec = (reinterpret_cast<uintptr_t>(rp) & (BF16_IN ? 7u : 15u)) == 0;
   const int n4 = vec ? N / 4 : 0;
-  for (int q = tid; q < n4; q += kTopkThreads) {
+  using V = typename std::conditional<BF16_IN, uint2, uint4>::type;
+  constexpr int kUnroll = BF16_IN ? 8 : 4;
+  const V* src = reinterpret_cast<const V*>(rp);
+  auto visit = [&](int q, const V& v) {
     if constexpr (BF16_IN) {
-      const uint2 v = __ldg(reinterpret_cast<const uint2*>(rp) + q);
       f(4 * q, order_key(v.x << 16));
       f(4 * q + 1, order_key(v.x & 0xffff0000u));
       f(4 * q + 2, order_key(v.y << 16));
       f(4 * q + 3, order_key(v.y & 0xffff0000u));
     } else {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(rp) + q);
       f(4 * q, order_key(v.x));
       f(4 * q + 1, order_key(v.y));
       f(4 * q + 2, order_key(v.z));
       f(4 * q + 3, order_key(v.w));
     }
+  };
+  int q = tid;
+  for (; q + (kUnroll - 1) * kTopkThreads < n4; q += kUnroll * kTopkThreads) {
+    V v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) v[u] = __ldg(src + q + u * kTopkThreads);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) visit(q + u * kTopkThreads, v[u]);
   }
+  for (; q < n4; q += kTopkThreads) visit(q, __ldg(src + q));
   for (int j = 4 * n4 + tid; j < N; j += kTopkThreads) f(j, load_key<BF16_IN>(rp, j));
 }
 
@@ -138,12 +151,14 @@ __device__ __forceinline__ void topk_clear_hist(TopkShared& sh) {
 // Radix select of the sh.need-th largest among keys[0, n) in shared memory
 // (0 marks an empty slot, below every finite key; sh.need must not exceed
 // the non-zero keys): sh.prefix ends as its key, sh.need as the number of
-// keys equal to it still to take. The bits above the highest one where the
+// keys equal to it still to take. With max_digits, only that many 8-bit
+// digits are resolved: sh.prefix then holds the key's leading bits with the
+// rest zero, a lower bound of the key. The bits above the highest one where the
 // non-zero keys differ are fixed at once, so the 8-bit digits start where the
 // keys spread (the candidates of a row share their top bits, and a digit
 // they all share would pile every lane's count onto one counter).
 __device__ __forceinline__ void topk_select_in_smem(TopkShared& sh, const uint32_t* keys,
-                                                    uint32_t n) {
+                                                    uint32_t n, int max_digits = 4) {
   const int tid = threadIdx.x, warp = tid >> 5;
   if (tid == 0) {
     sh.kmin = ~0u;
@@ -178,7 +193,7 @@ __device__ __forceinline__ void topk_select_in_smem(TopkShared& sh, const uint32
     sh.mask = common;
   }
   int hi = p + 1;  // bits [0, hi) are still free
-  while (hi > 0) {
+  for (int d = 0; hi > 0 && d < max_digits; ++d) {
     const int shift = hi > 8 ? hi - 8 : 0;
     const uint32_t width_mask = (1u << (hi - shift)) - 1u;
     topk_clear_hist(sh);
@@ -231,8 +246,12 @@ __device__ bool topk_sample_select(TopkShared& sh, const char* rp, int N, int k,
   uint32_t t_est = kNegInfKey + 1u;  // every finite value
   if (r <= nfin) {
     if (tid == 0) sh.need = r;
-    topk_select_in_smem(sh, sh.cand_key, kTopkCand);
-    t_est = sh.prefix;
+    // Two digits below the sample's common bits place the threshold within
+    // 1/65536 of the sample's key range under its r-th largest key; the few
+    // extra columns this admits cost nothing, and the exact selection below
+    // needs no exact threshold.
+    topk_select_in_smem(sh, sh.cand_key, kTopkCand, 2);
+    t_est = max(sh.prefix, kNegInfKey + 1u);  // never admit -inf
   }
   __syncthreads();
   if (tid == 0) {
@@ -273,8 +292,10 @@ __device__ bool topk_sample_select(TopkShared& sh, const char* rp, int N, int k,
   return true;
 }
 
+// Four CTAs per SM (the register cap this implies costs a few spills): the
+// shared-memory phases of one row then overlap the sweeps of the others.
 template <bool BF16_IN>
-__global__ void __launch_bounds__(kTopkThreads)
+__global__ void __launch_bounds__(kTopkThreads, 4)
     topk_rows_kernel(const void* __restrict__ logits, int64_t row_stride, int N, int k,
                      int32_t* __restrict__ idx, int64_t idx_stride) {
   __shared__ TopkShared sh;
