@@ -6,12 +6,13 @@
 // threshold any subset of the right size is taken.
 //
 // One CTA per row. Fast path: a sample of the row in shared memory sets a
-// threshold just below the expected k-th value, one sweep compacts the
-// columns above it (~1.2 k), and the selection finishes in shared memory.
+// threshold a little below the expected k-th value, one sweep compacts the
+// columns above it (k plus about three standard deviations of the sample's
+// estimate), and the selection finishes in shared memory.
 // Exact path (when the sample misjudges): radix select on an order-preserving
 // 32-bit key of the value, 8 bits per digit from the top. Sweep 1 histograms the top digit and
-// sweep 2 the second one among the elements matching it (per-warp
-// sub-histograms in shared memory); each picks the digit where the count from
+// sweep 2 the second one among the elements matching it (one 256-bin
+// histogram in shared memory); each picks the digit where the count from
 // the top reaches the number still to select. Sweep 3 writes the columns
 // whose top 16 bits are above the threshold's and compacts the ones equal to
 // it (the boundary bin, typically a few hundred) into shared memory, where
@@ -83,35 +84,31 @@ __device__ __forceinline__ void for_each_key(const char* rp, int N, F&& f) {
 }
 
 struct TopkShared {
-  uint32_t hist[kTopkWarps][256];
-  uint32_t total[256];
+  uint32_t hist[256];
   uint32_t cand_key[kTopkCand];
   int32_t cand_idx[kTopkCand];
   uint32_t prefix, mask, need, finite, out, ties, ncand;
   uint32_t kmin, kmax;
 };
 
-// Sum the per-warp histograms, then (warp 0) fix the digit at `shift` where
-// the count from the top reaches sh.need: lane l owns digits 8l .. 8l+7 and a
-// suffix sum over the lanes gives the count above each lane. Records the
-// number of finite candidates in sh.finite when asked. Ends with a barrier.
+// Warp 0 fixes the digit at `shift` where the histogram's count from the
+// top reaches sh.need: lane l owns digits 8l .. 8l+7 and a suffix sum over
+// the lanes gives the count above each lane. Records the number of finite
+// candidates in sh.finite when asked. Ends with a barrier.
+//
+// One histogram for the whole block measured faster than per-warp copies
+// (which spread the atomics but cost a summation and a larger clear each
+// digit): the keys a digit counts are spread over its bins.
 __device__ __forceinline__ void topk_pick_digit(TopkShared& sh, int shift, bool count_finite,
                                                 uint32_t digit_mask = 255u) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  __syncthreads();
-  if (tid < 256) {
-    uint32_t c = 0;
-#pragma unroll
-    for (int w = 0; w < kTopkWarps; ++w) c += sh.hist[w][tid];
-    sh.total[tid] = c;
-  }
   __syncthreads();
   if (warp == 0) {
     const uint32_t need = sh.need, prefix = sh.prefix, mask = sh.mask;
     uint32_t c[8], own = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      c[i] = sh.total[8 * lane + i];
+      c[i] = sh.hist[8 * lane + i];
       own += c[i];
     }
     uint32_t suffix = own;  // this lane and the ones above
@@ -144,7 +141,7 @@ __device__ __forceinline__ void topk_pick_digit(TopkShared& sh, int shift, bool 
 }
 
 __device__ __forceinline__ void topk_clear_hist(TopkShared& sh) {
-  for (int i = threadIdx.x; i < kTopkWarps * 256; i += kTopkThreads) (&sh.hist[0][0])[i] = 0;
+  for (int i = threadIdx.x; i < 256; i += kTopkThreads) sh.hist[i] = 0;
   __syncthreads();
 }
 
@@ -159,7 +156,7 @@ __device__ __forceinline__ void topk_clear_hist(TopkShared& sh) {
 // they all share would pile every lane's count onto one counter).
 __device__ __forceinline__ void topk_select_in_smem(TopkShared& sh, const uint32_t* keys,
                                                     uint32_t n, int max_digits = 4) {
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x;
   if (tid == 0) {
     sh.kmin = ~0u;
     sh.kmax = 0u;
@@ -201,7 +198,7 @@ __device__ __forceinline__ void topk_select_in_smem(TopkShared& sh, const uint32
     for (uint32_t c = tid; c < n; c += kTopkThreads) {
       const uint32_t key = keys[c];
       if (key != 0u && (key & mask) == prefix)
-        atomicAdd(&sh.hist[warp][(key >> shift) & width_mask], 1u);
+        atomicAdd(&sh.hist[(key >> shift) & width_mask], 1u);
     }
     topk_pick_digit(sh, shift, false, width_mask);
     hi = shift;
@@ -240,9 +237,12 @@ __device__ bool topk_sample_select(TopkShared& sh, const char* rp, int N, int k,
   atomicAdd(&sh.ncand, nfin_local);
   __syncthreads();
   const uint32_t nfin = sh.ncand;
-  // the sample rank expected to have ~1.2 k columns of the row at or above it
-  const uint32_t r = static_cast<uint32_t>(ceilf(1.2f * static_cast<float>(k) *
-                                                 static_cast<float>(ns) / static_cast<float>(N))) + 4u;
+  // The sample rank m = k * ns / N is expected to have k columns of the row
+  // at or above it; its count among the sample varies by about sqrt(m), so
+  // the threshold goes to rank m + 3 sqrt(m) (+4), which leaves fewer than k
+  // columns above it only rarely (the exact path then redoes the row).
+  const float m = static_cast<float>(k) * static_cast<float>(ns) / static_cast<float>(N);
+  const uint32_t r = static_cast<uint32_t>(ceilf(m + 3.f * sqrtf(m))) + 4u;
   uint32_t t_est = kNegInfKey + 1u;  // every finite value
   if (r <= nfin) {
     if (tid == 0) sh.need = r;
@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(kTopkThreads, 4)
     topk_rows_kernel(const void* __restrict__ logits, int64_t row_stride, int N, int k,
                      int32_t* __restrict__ idx, int64_t idx_stride) {
   __shared__ TopkShared sh;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x;
   const int64_t row = blockIdx.x;
   const char* rp = reinterpret_cast<const char*>(logits) + row * row_stride * (BF16_IN ? 2 : 4);
   int32_t* out = idx + row * idx_stride;
@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(kTopkThreads, 4)
     const uint32_t prefix = sh.prefix, mask = sh.mask;
     for_each_key<BF16_IN>(rp, N, [&](int, uint32_t key) {
       if (key > kNegInfKey && (key & mask) == prefix)
-        atomicAdd(&sh.hist[warp][(key >> shift) & 255u], 1u);
+        atomicAdd(&sh.hist[(key >> shift) & 255u], 1u);
     });
     topk_pick_digit(sh, shift, pass == 0);
     if (sh.finite <= static_cast<uint32_t>(k)) break;
@@ -362,12 +362,12 @@ __global__ void __launch_bounds__(kTopkThreads, 4)
       if (in_smem) {
         for (uint32_t c = tid; c < nc; c += kTopkThreads) {
           const uint32_t key = sh.cand_key[c];
-          if ((key & mask) == prefix) atomicAdd(&sh.hist[warp][(key >> shift) & 255u], 1u);
+          if ((key & mask) == prefix) atomicAdd(&sh.hist[(key >> shift) & 255u], 1u);
         }
       } else {
         for_each_key<BF16_IN>(rp, N, [&](int, uint32_t key) {
           if (key > kNegInfKey && (key & mask) == prefix)
-            atomicAdd(&sh.hist[warp][(key >> shift) & 255u], 1u);
+            atomicAdd(&sh.hist[(key >> shift) & 255u], 1u);
         });
       }
       topk_pick_digit(sh, shift, false);
