@@ -33,11 +33,12 @@
 //               copy the tile's key scale factors into shared memory in the
 //               transposed order the TMEM copy wants (4-byte cp.async each)
 //  warp 1       TMEM allocator + MMA issuer (one lane)
-//  warp 2       unit scheduler: claims units two ahead and prefetches their
-//               windows, head weights and (MX) Q scale factors into
-//               registers; when a slot frees it stages the weights in shared
-//               memory as FP32 (and the Q scale factors) and starts the TMA
-//               of the unit's Q block, one unit ahead of the MMA
+//  warp 2       unit scheduler: claims a unit and fetches its windows, head
+//               weights and (MX) Q scale factors into registers; when the Q
+//               half of a slot frees it starts the TMA of the unit's Q block
+//               (and stages the Q scale factors), when the epilogue half
+//               frees it stages the weights in shared memory as FP32 and the
+//               windows, one unit ahead of the MMA
 //  warp 3       idle
 //  warps 4..    epilogue, R = 1 or 2 query rows per warp (a per-format
 //               choice): warp w reads TMEM lanes 32*(w%4)..+31 (the
@@ -87,6 +88,14 @@ struct UnitInfo {
   int32_t flags;     // bit 0: fill [0, t0*128) with -inf; bit 1: fill [t1*128, N)
   int32_t lo[4];     // clamped window per row
   int32_t hi[4];
+};
+
+// What the K producer and the MMA issuer need of a unit, published with its
+// Q block (the rest of UnitInfo and the weights are the epilogue's).
+struct QInfo {
+  int32_t stop;
+  int32_t b;
+  int32_t c0, c1;
 };
 
 struct KernelParams {
@@ -206,9 +215,10 @@ struct Layout {
   static constexpr int kSfaOff = kWOff + 2 * kWBytes;
   static constexpr int kSfbOff = kSfaOff + (T::kMX ? T::kStages * kSfaBytes : 0);
   static constexpr int kInfoOff = kSfbOff + (T::kMX ? 2 * kSfbBytes : 0);
-  static constexpr int kBarOff = kInfoOff + 2 * (int)sizeof(UnitInfo);
+  static constexpr int kQInfoOff = kInfoOff + 2 * (int)sizeof(UnitInfo);
+  static constexpr int kBarOff = kQInfoOff + 2 * (int)sizeof(QInfo);
   static constexpr int kNumBars =
-      2 + 2 + 2 * T::kStages + 2 * kAccBufs + (T::kMX ? T::kStages : 0) + 1;
+      2 + 2 + 2 * T::kStages + 2 * kAccBufs + (T::kMX ? T::kStages : 0) + 1 + 2 + 2;
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
   static constexpr int kBytes = kMiscOff + 16;
   static_assert(kBytes <= 232448, "shared memory budget");
@@ -337,7 +347,14 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
   uint8_t* sfa_s = smem + L::kSfaOff;  // [kStages][128 keys x 4 bytes], TMEM-copy order
   uint8_t* sfb_s = smem + L::kSfbOff;  // [2 slots][256 rows x 4 bytes], TMEM-copy order
   UnitInfo* info = reinterpret_cast<UnitInfo*>(smem + L::kInfoOff);
+  QInfo* qinfo = reinterpret_cast<QInfo*>(smem + L::kQInfoOff);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  // A unit slot has two halves: the Q half (Q block, MX Q scales, QInfo;
+  // q_full / q_empty), read by the K producer and the MMA issuer and
+  // released by the MMA's commit, and the epilogue half (UnitInfo, weights;
+  // unit_full / unit_empty), released by the epilogue warps. The Q half of
+  // a slot is thus refilled as soon as the MMAs of its previous unit are
+  // done, a tile or two before the epilogue is.
   uint64_t* unit_full = bars;
   uint64_t* unit_empty = bars + 2;
   uint64_t* k_full = bars + 4;
@@ -346,6 +363,8 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
   uint64_t* acc_empty = acc_full + kAccBufs;
   uint64_t* sf_full = acc_empty + kAccBufs;  // MX only
   uint64_t* drain = sf_full + (T::kMX ? T::kStages : 0);  // MMA issuer, after an abort
+  uint64_t* q_full = drain + 1;
+  uint64_t* q_empty = q_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
 
@@ -359,8 +378,10 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
     }
     *abort_flag = 0;
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&unit_full[s], 1);  // the scheduler's arrive (+ the Q TMA bytes)
-      mbar_init(&unit_empty[s], 2 + kNumEpiWarps);  // K producer, MMA commit, epilogue warps
+      mbar_init(&unit_full[s], 1);                // the scheduler's arrive
+      mbar_init(&unit_empty[s], kNumEpiWarps);    // epilogue warps
+      mbar_init(&q_full[s], 1);                   // the scheduler's arrive + the Q TMA bytes
+      mbar_init(&q_empty[s], 1);                  // the MMA issuer's commit
     }
     for (int s = 0; s < kAccBufs; ++s) {
       mbar_init(&acc_full[s], 1);
@@ -389,9 +410,10 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
   } else if (warp == 2) {
     // ---------------------------------------------------------- unit scheduler
     // A unit is claimed and its rows, windows, weights and (MX) Q scale
-    // words are fetched into registers; once its slot is free, lane 0 writes
-    // the unit info and starts the Q TMA and all 32 lanes store the weights
-    // (FP32) and scale words into the slot. Claiming and fetching take
+    // words are fetched into registers; once the Q half of its slot is free,
+    // lane 0 writes the QInfo and starts the Q TMA and all lanes store the
+    // scale words; once the epilogue half is free, lane 0 writes the unit
+    // info and all lanes store the weights (FP32). Claiming and fetching take
     // several microseconds (a contended atomic, then dependent global
     // loads). With grouped rows (one more dependent load, the row order;
     // many short units) the next unit is claimed as soon as a slot frees
@@ -496,27 +518,36 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       if (lane == 0) u_next = atomicAdd(p.scratch + 0, 1);
       prepare(__shfl_sync(0xffffffffu, u_next, 0), cur);
     }
+    // Waits for a slot half; on expiry, lets the Q loads still in flight
+    // (units [first, last)) land before the CTA exits.
+    auto wait_half = [&](uint64_t* bar, uint32_t it, uint32_t first, uint32_t last) {
+      int ok = 1;
+      if (lane == 0) {
+        ok = mbar_wait(&bar[it & 1], ((it >> 1) & 1) ^ 1, abort_flag, p.timeout_ns);
+        if (!ok) {
+          raise_error(p.scratch, abort_flag, kErrTimeout);
+          for (uint32_t j = first; j < last; ++j)
+            mbar_wait_drain(&q_full[j & 1], (j >> 1) & 1, p.timeout_ns);
+        }
+      }
+      return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    };
     for (uint32_t it = 0;; ++it) {
       const int slot = it & 1;
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait(&unit_empty[slot], ((it >> 1) & 1) ^ 1, abort_flag, p.timeout_ns);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) {
-        if (lane == 0) {
-          raise_error(p.scratch, abort_flag, kErrTimeout);
-          // Let the Q loads of the units still in the slots land before the
-          // CTA exits.
-          for (uint32_t j = it > 2 ? it - 2 : 0; j < it; ++j)
-            mbar_wait_drain(&unit_full[j & 1], (j >> 1) & 1, p.timeout_ns);
-        }
-        break;
-      }
+      // Q half: free once the MMAs of unit it-2 are done.
+      if (!wait_half(q_empty, it, it > 2 ? it - 2 : 0, it)) break;
       if (!ahead) {
         if (lane == 0) u_next = atomicAdd(p.scratch + 0, 1);
         prepare(__shfl_sync(0xffffffffu, u_next, 0), cur);
       }
+      QInfo& qi = qinfo[slot];
       UnitInfo& in = info[slot];
       if (cur.u >= p.num_units) {
+        if (lane == 0) {
+          qi.stop = 1;
+          mbar_arrive(&q_full[slot]);
+        }
+        if (!wait_half(unit_empty, it, it > 1 ? it - 1 : 0, it)) break;
         if (lane == 0) {
           in.stop = 1;
           mbar_arrive(&unit_full[slot]);
@@ -526,9 +557,12 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       // The next claim; its result is first needed after this unit is out.
       if (ahead && lane == 0) u_next = atomicAdd(p.scratch + 0, 1);
       if (lane == 0) {
-        in = cur.in;
+        qi.stop = 0;
+        qi.b = cur.in.b;
+        qi.c0 = cur.in.c0;
+        qi.c1 = cur.in.c1;
         if (cur.in.c1 > cur.in.c0) {
-          mbar_expect_tx(&unit_full[slot], L::kQBlockBytes);
+          mbar_expect_tx(&q_full[slot], L::kQBlockBytes);
           // One 64-head box per row and panel; row r lands at rows 64r.. of
           // the block (a whole number of swizzle atoms).
           uint8_t* qdst = qbuf + slot * L::kQBlockBytes;
@@ -537,18 +571,9 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
 #pragma unroll
             for (int pnl = 0; pnl < L::kPanels; ++pnl)
               tma_load_2d(qdst + pnl * L::kQPanelBytes + r * kHeads * T::kSwizzleBytes,
-                          &p.tmap_q, &unit_full[slot], pnl * (T::kSwizzleBytes / T::kTmaElemBytes),
+                          &p.tmap_q, &q_full[slot], pnl * (T::kSwizzleBytes / T::kTmaElemBytes),
                           cur.grow[r] * kHeads, pol_first);
         }
-      }
-      // Head weights of the 4 rows as FP32, row-major 4 x 64.
-      float4* wdst = reinterpret_cast<float4*>(wbuf + slot * L::kWBytes);
-      if (p.w_bf16) {
-        wdst[2 * lane] = cur.w[0];
-        wdst[2 * lane + 1] = cur.w[1];
-      } else {
-        wdst[lane] = cur.w[0];
-        wdst[lane + 32] = cur.w[1];
       }
       if constexpr (T::kMX) {
         // Q scale word of (row, head) m = 32c + lane goes to TMEM lane m % 32,
@@ -560,6 +585,20 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
           const int m = 32 * c + lane;
           *reinterpret_cast<uint32_t*>(dst + (m >> 7) * 512 + 16 * lane + 4 * (c & 3)) = cur.sf[c];
         }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_full[slot]);
+      // Epilogue half: free once the epilogue is done with unit it-2.
+      if (!wait_half(unit_empty, it, it > 1 ? it - 1 : 0, it + 1)) break;
+      if (lane == 0) in = cur.in;
+      // Head weights of the 4 rows as FP32, row-major 4 x 64.
+      float4* wdst = reinterpret_cast<float4*>(wbuf + slot * L::kWBytes);
+      if (p.w_bf16) {
+        wdst[2 * lane] = cur.w[0];
+        wdst[2 * lane + 1] = cur.w[1];
+      } else {
+        wdst[lane] = cur.w[0];
+        wdst[lane + 32] = cur.w[1];
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&unit_full[slot]);
@@ -576,18 +615,20 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
     for (uint32_t it = 0;; ++it) {
       const int slot = it & 1;
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(&unit_full[slot], (it >> 1) & 1, abort_flag, p.timeout_ns);
+      if (lane == 0) ok = mbar_wait(&q_full[slot], (it >> 1) & 1, abort_flag, p.timeout_ns);
       if constexpr (T::kMX) {
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        __syncwarp();  // lane 0's acquire covers the unit info the other lanes read
+        __syncwarp();  // lane 0's acquire covers the QInfo the other lanes read
       }
       if (!ok) {
         if (lane == 0) raise_error(p.scratch, abort_flag, kErrTimeout);
         break;
       }
-      const UnitInfo& in = info[slot];
-      if (in.stop) break;
-      const int c0 = in.c0, c1 = in.c1, b = in.b;
+      // Read once, at the unit's start: the slot's Q half is refilled only
+      // after the MMAs of this unit, which consume every tile loaded here.
+      const QInfo& qi = qinfo[slot];
+      if (qi.stop) break;
+      const int c0 = qi.c0, c1 = qi.c1, b = qi.b;
       for (int t = c0; t < c1; ++t, ++kiter) {
         const int st = kiter % T::kStages;
         if (lane == 0)
@@ -642,7 +683,6 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         if (lane == 0) raise_error(p.scratch, abort_flag, kErrTimeout);
         break;
       }
-      if (lane == 0) mbar_arrive(&unit_empty[slot]);
     }
     if (*abort_flag && lane == 0) {
       // Let the key tiles (and scale copies) of the last kStages issues land
@@ -669,13 +709,13 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
     const uint64_t sfb_desc0 = smem_desc(smem_u32(sfb_s), 128, 0);
     for (uint32_t it = 0;; ++it) {
       const int slot = it & 1;
-      if (!mbar_wait(&unit_full[slot], (it >> 1) & 1, abort_flag, p.timeout_ns)) {
+      if (!mbar_wait(&q_full[slot], (it >> 1) & 1, abort_flag, p.timeout_ns)) {
         raise_error(p.scratch, abort_flag, kErrTimeout);
         break;
       }
-      const UnitInfo& in = info[slot];
-      if (in.stop) break;
-      const int c0 = in.c0, c1 = in.c1;
+      const QInfo& qi = qinfo[slot];
+      if (qi.stop) break;
+      const int c0 = qi.c0, c1 = qi.c1;
       const uint64_t b_base = q_desc0 + ((slot * L::kQBlockBytes) >> 4);
       bool ok = true;
       for (int t = c0; t < c1; ++t, ++kiter, ++aiter) {
@@ -740,7 +780,9 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         raise_error(p.scratch, abort_flag, kErrTimeout);
         break;
       }
-      tc_commit(&unit_empty[slot]);
+      // The slot's Q half (Q block, Q scales, QInfo) is free once these MMAs
+      // and scale copies are done.
+      tc_commit(&q_empty[slot]);
     }
     if (*abort_flag) {
       // A commit tracks every MMA and TMEM copy this thread issued: wait for
