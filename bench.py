@@ -44,15 +44,15 @@ L2_FLUSH_BYTES = 256 << 20
 # workload, with the digest of the kernel sources it was taken on (see
 # profiles/). Reported as roofline.traffic only while the sources still match.
 PROFILED_TRAFFIC = {
-    "bf16_batched_causal_4096": ("a43bdc39de6c89fb", 137.464832e6 + 80.025856e6),
-    "fp8_per_token_2048x32768": ("a43bdc39de6c89fb", 21.675264e6 + 208.331008e6),
-    "mxfp8_2048x32768": ("a43bdc39de6c89fb", 22.209536e6 + 207.915264e6),
-    "mxfp4_2048x32768": ("a43bdc39de6c89fb", 11.813376e6 + 208.038656e6),
-    "paged_fp8_decode_64x2_32768": ("a43bdc39de6c89fb", 208.301824e6 + 11.921152e6),
-    "mxfp8_8192x65536": ("a43bdc39de6c89fb", 81144064 + 2088112640),
-    "mxfp4_8192x65536": ("a43bdc39de6c89fb", 42804480 + 2087783424),
-    "mxfp4_irregular_8192x65536": ("a43bdc39de6c89fb", 42277120 + 2085999616),
-    "thd_bf16_3seq_8192x32768": ("a43bdc39de6c89fb", 144849920 + 1012862720),
+    "bf16_batched_causal_4096": ("a0ab85169a9d316f", 137.495040e6 + 79.709440e6),
+    "fp8_per_token_2048x32768": ("a0ab85169a9d316f", 21.721088e6 + 207.723008e6),
+    "mxfp8_2048x32768": ("a0ab85169a9d316f", 22.222592e6 + 207.570432e6),
+    "mxfp4_2048x32768": ("a0ab85169a9d316f", 11.900160e6 + 207.955968e6),
+    "paged_fp8_decode_64x2_32768": ("a0ab85169a9d316f", 208.284160e6 + 11.974400e6),
+    "mxfp8_8192x65536": ("a0ab85169a9d316f", 80375552 + 2087707904),
+    "mxfp4_8192x65536": ("a0ab85169a9d316f", 42581504 + 2087260416),
+    "mxfp4_irregular_8192x65536": ("a0ab85169a9d316f", 43101952 + 2086262272),
+    "thd_bf16_3seq_8192x32768": ("a0ab85169a9d316f", 145004800 + 1013174528),
 }
 
 
