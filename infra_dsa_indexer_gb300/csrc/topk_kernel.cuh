@@ -27,7 +27,6 @@
 namespace dsa {
 
 constexpr int kTopkThreads = 512;
-constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kTopkCand = 3840;  // candidate entries kept in shared memory
 
 // Larger value -> larger key; -inf -> 0x007fffff, below every finite value.
