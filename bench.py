@@ -81,6 +81,8 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="--impl reference: CPU seconds all its steps together aim for")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--topk", type=int, default=0,
@@ -234,7 +236,7 @@ def run_reference(args, _dist):
     case = synth.make_workload(args.workload)
     import oracle
     oracle.build()
-    budget = 120.0 / max(1, args.steps + args.warmup)   # seconds per step
+    budget = args.ref_seconds / max(1, args.steps + args.warmup)   # seconds per step
     nth = oracle.num_threads()
     lo = np.clip(case.ks.reshape(-1).astype(np.int64), 0, case.N)
     hi = np.clip(case.ke.reshape(-1).astype(np.int64), 0, case.N)

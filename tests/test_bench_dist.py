@@ -6,6 +6,7 @@ around the timed region and the maximum of the per-rank times. Both are
 checked here with two gloo ranks, plus the reference arm's rule that only
 rank 0 runs the oracle.
 """
+import json
 import multiprocessing as mp
 import os
 import socket
@@ -67,3 +68,23 @@ def test_reference_arm_runs_on_rank0_only(monkeypatch, capsys):
     monkeypatch.setenv("RANK", "0")
     bench.main(["--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"])
     assert len(called) == 1
+
+
+def test_reference_arm_json_line(monkeypatch, capsys):
+    """The reference arm (the float64 oracle on sampled rows) prints one JSON
+    line with the keys the bench contract asks of it."""
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    bench.main(["--impl", "reference", "--workload", "tiny_causal_bf16", "--steps", "2",
+                "--warmup", "3", "--ref-seconds", "1.0"])
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["higher_is_better"] is True
+    assert d["steps"] == 2 and d["warmup"] == 3 and d["n_gpus"] == 1 and d["dtype"] == "f64"
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["config"]["workload"] == "tiny_causal_bf16"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
