@@ -206,7 +206,7 @@ __device__ __forceinline__ void topk_select_in_smem(TopkShared& sh, const uint32
 }
 
 // Fast path (sample select). Runs of 8 consecutive columns spread over the
-// row (at most kTopkCand keys, in shared memory) give a threshold a little
+// row (in shared memory) give a threshold a little
 // below the expected k-th largest value; one sweep compacts every column at
 // or above it, and the exact selection runs on those in shared memory.
 // Returns false, with nothing written, when the sample misjudged: fewer than
@@ -216,8 +216,15 @@ template <bool BF16_IN>
 __device__ bool topk_sample_select(TopkShared& sh, const char* rp, int N, int k, int32_t* out) {
   const int tid = threadIdx.x;
   constexpr int kRun = 8;
-  constexpr int kRuns = kTopkCand / kRun;
-  const int step = N >= kRun * kRuns ? (N / kRuns) / kRun * kRun : kRun;
+  // Sample size: enough runs that the k-th column's expected sample rank,
+  // m = k * ns / N, is about 128 (spread ~9%), at least 512 keys and at
+  // most the candidate buffer. A larger sample only lengthens the shared-
+  // memory select; a smaller one sends more rows to the exact path.
+  const int64_t want_runs = ((128LL * N + max(k, 1) - 1) / max(k, 1) + kRun - 1) / kRun;
+  const int runs =
+      static_cast<int>(want_runs < 64 ? 64 : (want_runs > kTopkCand / kRun ? kTopkCand / kRun
+                                                                            : want_runs));
+  const int step = N >= kRun * runs ? (N / runs) / kRun * kRun : kRun;
   if (tid == 0) {
     sh.ncand = 0;
     sh.prefix = 0;
@@ -225,14 +232,14 @@ __device__ bool topk_sample_select(TopkShared& sh, const char* rp, int N, int k,
   }
   __syncthreads();
   uint32_t nfin_local = 0;
-  for (int s = tid; s < kTopkCand; s += kTopkThreads) {
+  for (int s = tid; s < runs * kRun; s += kTopkThreads) {
     const int j = (s / kRun) * step + s % kRun;
     const uint32_t key = j < N ? load_key<BF16_IN>(rp, j) : 0u;
     const bool fin = key > kNegInfKey;
     sh.cand_key[s] = fin ? key : 0u;  // 0 ranks below every finite key
     nfin_local += fin ? 1u : 0u;
   }
-  const int ns = min(N, kRuns * step) / step * kRun + min(kRun, min(N, kRuns * step) % step);
+  const int ns = min(N, runs * step) / step * kRun + min(kRun, min(N, runs * step) % step);
   atomicAdd(&sh.ncand, nfin_local);
   __syncthreads();
   const uint32_t nfin = sh.ncand;
@@ -249,7 +256,7 @@ __device__ bool topk_sample_select(TopkShared& sh, const char* rp, int N, int k,
     // 1/65536 of the sample's key range under its r-th largest key; the few
     // extra columns this admits cost nothing, and the exact selection below
     // needs no exact threshold.
-    topk_select_in_smem(sh, sh.cand_key, kTopkCand, 2);
+    topk_select_in_smem(sh, sh.cand_key, runs * kRun, 2);
     t_est = max(sh.prefix, kNegInfKey + 1u);  // never admit -inf
   }
   __syncthreads();
