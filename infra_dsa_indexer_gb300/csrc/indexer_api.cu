@@ -449,20 +449,35 @@ int indexer_topk(const void* logits, int logits_bf16, int64_t rows, int32_t N,
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return IDX_ERR_CUDA;
+  int sms = 0;
   {
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceInfo* di = nullptr;
     int st = get_device_info(dev, &di);
     if (st) return st;
     if (di->cc_major != 10 || di->cc_minor != 3) return IDX_ERR_DEVICE;
+    sms = di->sm_count;
   }
+  // One CTA per row; rows that cannot fill the GPU at 512 threads and four
+  // CTAs per SM get 1024 threads each.
   const dim3 grid(static_cast<unsigned>(rows));
-  if (logits_bf16)
-    dsa::topk_rows_kernel<true><<<grid, dsa::kTopkThreads, 0, stream>>>(logits, row_stride, N, k,
-                                                                        idx, idx_stride);
-  else
-    dsa::topk_rows_kernel<false><<<grid, dsa::kTopkThreads, 0, stream>>>(logits, row_stride, N,
-                                                                         k, idx, idx_stride);
+  const bool few = rows <= 2LL * sms;
+  constexpr int kMany = dsa::kTopkThreads, kFew = dsa::kTopkThreadsFew;
+  if (logits_bf16) {
+    if (few)
+      dsa::topk_rows_kernel<kFew, true><<<grid, kFew, 0, stream>>>(logits, row_stride, N, k, idx,
+                                                                  idx_stride);
+    else
+      dsa::topk_rows_kernel<kMany, true><<<grid, kMany, 0, stream>>>(logits, row_stride, N, k,
+                                                                    idx, idx_stride);
+  } else {
+    if (few)
+      dsa::topk_rows_kernel<kFew, false><<<grid, kFew, 0, stream>>>(logits, row_stride, N, k,
+                                                                   idx, idx_stride);
+    else
+      dsa::topk_rows_kernel<kMany, false><<<grid, kMany, 0, stream>>>(logits, row_stride, N, k,
+                                                                     idx, idx_stride);
+  }
   return cudaGetLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }
 

@@ -26,7 +26,8 @@
 
 namespace dsa {
 
-constexpr int kTopkThreads = 512;
+constexpr int kTopkThreads = 512;       // threads per CTA, four CTAs per SM
+constexpr int kTopkThreadsFew = 1024;   // when the rows do not fill the GPU
 constexpr int kTopkCand = 3840;  // candidate entries kept in shared memory
 
 // Larger value -> larger key; -inf -> 0x007fffff, below every finite value.
@@ -49,7 +50,7 @@ __device__ __forceinline__ uint32_t load_key(const void* row, int j) {
 // when the row start is 16-byte aligned (FP32) or 8-byte aligned (BF16).
 // The loads of kUnroll consecutive strides are issued before any key is
 // visited, so each CTA keeps 32 KB of its row in flight.
-template <bool BF16_IN, typename F>
+template <int NT, bool BF16_IN, typename F>
 __device__ __forceinline__ void for_each_key(const char* rp, int N, F&& f) {
   const int tid = threadIdx.x;
   const bool vec = (reinterpret_cast<uintptr_t>(rp) & (BF16_IN ? 7u : 15u)) == 0;
@@ -71,15 +72,15 @@ __device__ __forceinline__ void for_each_key(const char* rp, int N, F&& f) {
     }
   };
   int q = tid;
-  for (; q + (kUnroll - 1) * kTopkThreads < n4; q += kUnroll * kTopkThreads) {
+  for (; q + (kUnroll - 1) * NT < n4; q += kUnroll * NT) {
     V v[kUnroll];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) v[u] = __ldg(src + q + u * kTopkThreads);
+    for (int u = 0; u < kUnroll; ++u) v[u] = __ldg(src + q + u * NT);
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) visit(q + u * kTopkThreads, v[u]);
+    for (int u = 0; u < kUnroll; ++u) visit(q + u * NT, v[u]);
   }
-  for (; q < n4; q += kTopkThreads) visit(q, __ldg(src + q));
-  for (int j = 4 * n4 + tid; j < N; j += kTopkThreads) f(j, load_key<BF16_IN>(rp, j));
+  for (; q < n4; q += NT) visit(q, __ldg(src + q));
+  for (int j = 4 * n4 + tid; j < N; j += NT) f(j, load_key<BF16_IN>(rp, j));
 }
 
 struct TopkShared {
@@ -139,8 +140,9 @@ __device__ __forceinline__ void topk_pick_digit(TopkShared& sh, int shift, bool 
   __syncthreads();
 }
 
+template <int NT>
 __device__ __forceinline__ void topk_clear_hist(TopkShared& sh) {
-  for (int i = threadIdx.x; i < 256; i += kTopkThreads) sh.hist[i] = 0;
+  for (int i = threadIdx.x; i < 256; i += NT) sh.hist[i] = 0;
   __syncthreads();
 }
 
@@ -153,6 +155,7 @@ __device__ __forceinline__ void topk_clear_hist(TopkShared& sh) {
 // non-zero keys differ are fixed at once, so the 8-bit digits start where the
 // keys spread (the candidates of a row share their top bits, and a digit
 // they all share would pile every lane's count onto one counter).
+template <int NT>
 __device__ __forceinline__ void topk_select_in_smem(TopkShared& sh, const uint32_t* keys,
                                                     uint32_t n, int max_digits = 4) {
   const int tid = threadIdx.x;
@@ -162,7 +165,7 @@ __device__ __forceinline__ void topk_select_in_smem(TopkShared& sh, const uint32
   }
   __syncthreads();
   uint32_t mn = ~0u, mx = 0u;
-  for (uint32_t c = tid; c < n; c += kTopkThreads) {
+  for (uint32_t c = tid; c < n; c += NT) {
     const uint32_t key = keys[c];
     if (key != 0u) {
       mn = min(mn, key);
@@ -192,9 +195,9 @@ __device__ __forceinline__ void topk_select_in_smem(TopkShared& sh, const uint32
   for (int d = 0; hi > 0 && d < max_digits; ++d) {
     const int shift = hi > 8 ? hi - 8 : 0;
     const uint32_t width_mask = (1u << (hi - shift)) - 1u;
-    topk_clear_hist(sh);
+    topk_clear_hist<NT>(sh);
     const uint32_t prefix = sh.prefix, mask = sh.mask;
-    for (uint32_t c = tid; c < n; c += kTopkThreads) {
+    for (uint32_t c = tid; c < n; c += NT) {
       const uint32_t key = keys[c];
       if (key != 0u && (key & mask) == prefix)
         atomicAdd(&sh.hist[(key >> shift) & width_mask], 1u);
@@ -212,7 +215,7 @@ __device__ __forceinline__ void topk_select_in_smem(TopkShared& sh, const uint32
 // Returns false, with nothing written, when the sample misjudged: fewer than
 // k columns reach the threshold although it excluded finite values, or more
 // columns than fit.
-template <bool BF16_IN>
+template <int NT, bool BF16_IN>
 __device__ bool topk_sample_select(TopkShared& sh, const char* rp, int N, int k, int32_t* out) {
   const int tid = threadIdx.x;
   constexpr int kRun = 8;
@@ -232,7 +235,7 @@ __device__ bool topk_sample_select(TopkShared& sh, const char* rp, int N, int k,
   }
   __syncthreads();
   uint32_t nfin_local = 0;
-  for (int s = tid; s < runs * kRun; s += kTopkThreads) {
+  for (int s = tid; s < runs * kRun; s += NT) {
     const int j = (s / kRun) * step + s % kRun;
     const uint32_t key = j < N ? load_key<BF16_IN>(rp, j) : 0u;
     const bool fin = key > kNegInfKey;
@@ -256,7 +259,7 @@ __device__ bool topk_sample_select(TopkShared& sh, const char* rp, int N, int k,
     // 1/65536 of the sample's key range under its r-th largest key; the few
     // extra columns this admits cost nothing, and the exact selection below
     // needs no exact threshold.
-    topk_select_in_smem(sh, sh.cand_key, runs * kRun, 2);
+    topk_select_in_smem<NT>(sh, sh.cand_key, runs * kRun, 2);
     t_est = max(sh.prefix, kNegInfKey + 1u);  // never admit -inf
   }
   __syncthreads();
@@ -269,7 +272,7 @@ __device__ bool topk_sample_select(TopkShared& sh, const char* rp, int N, int k,
     sh.ties = 0;
   }
   __syncthreads();
-  for_each_key<BF16_IN>(rp, N, [&](int j, uint32_t key) {
+  for_each_key<NT, BF16_IN>(rp, N, [&](int j, uint32_t key) {
     if (key < t_est) return;
     const uint32_t pos = atomicAdd(&sh.ncand, 1u);
     if (pos < static_cast<uint32_t>(kTopkCand)) {
@@ -283,13 +286,13 @@ __device__ bool topk_sample_select(TopkShared& sh, const char* rp, int N, int k,
   if (nc < static_cast<uint32_t>(k)) {
     // right only when the threshold let every finite value through
     if (t_est != kNegInfKey + 1u) return false;
-    for (uint32_t c = tid; c < nc; c += kTopkThreads) out[c] = sh.cand_idx[c];
-    for (int i = static_cast<int>(nc) + tid; i < k; i += kTopkThreads) out[i] = -1;
+    for (uint32_t c = tid; c < nc; c += NT) out[c] = sh.cand_idx[c];
+    for (int i = static_cast<int>(nc) + tid; i < k; i += NT) out[i] = -1;
     return true;
   }
-  topk_select_in_smem(sh, sh.cand_key, nc);
+  topk_select_in_smem<NT>(sh, sh.cand_key, nc);
   const uint32_t thr = sh.prefix, ties = sh.need;
-  for (uint32_t c = tid; c < nc; c += kTopkThreads) {
+  for (uint32_t c = tid; c < nc; c += NT) {
     const uint32_t key = sh.cand_key[c];
     bool t = key > thr;
     if (key == thr) t = atomicAdd(&sh.ties, 1u) < ties;
@@ -298,10 +301,13 @@ __device__ bool topk_sample_select(TopkShared& sh, const char* rp, int N, int k,
   return true;
 }
 
-// Four CTAs per SM (the register cap this implies costs a few spills): the
-// shared-memory phases of one row then overlap the sweeps of the others.
-template <bool BF16_IN>
-__global__ void __launch_bounds__(kTopkThreads, 4)
+// NT threads per CTA and 2048 / NT CTAs per SM (the register cap this
+// implies costs a few spills). With many rows, 512 threads and four CTAs
+// per SM: the shared-memory phases of one row overlap the sweeps of the
+// others. With too few rows to fill the GPU (decode), 1024 threads per row
+// shorten each row's sweeps and shared-memory passes instead.
+template <int NT, bool BF16_IN>
+__global__ void __launch_bounds__(NT, 2048 / NT)
     topk_rows_kernel(const void* __restrict__ logits, int64_t row_stride, int N, int k,
                      int32_t* __restrict__ idx, int64_t idx_stride) {
   __shared__ TopkShared sh;
@@ -309,7 +315,7 @@ __global__ void __launch_bounds__(kTopkThreads, 4)
   const int64_t row = blockIdx.x;
   const char* rp = reinterpret_cast<const char*>(logits) + row * row_stride * (BF16_IN ? 2 : 4);
   int32_t* out = idx + row * idx_stride;
-  if (topk_sample_select<BF16_IN>(sh, rp, N, k, out)) return;
+  if (topk_sample_select<NT, BF16_IN>(sh, rp, N, k, out)) return;
 
   // Exact path: radix select by sweeps over the row.
   __syncthreads();
@@ -326,9 +332,9 @@ __global__ void __launch_bounds__(kTopkThreads, 4)
   // Sweeps 1 and 2: the top two digits.
   for (int pass = 0; pass < 2; ++pass) {
     const int shift = 24 - 8 * pass;
-    topk_clear_hist(sh);
+    topk_clear_hist<NT>(sh);
     const uint32_t prefix = sh.prefix, mask = sh.mask;
-    for_each_key<BF16_IN>(rp, N, [&](int, uint32_t key) {
+    for_each_key<NT, BF16_IN>(rp, N, [&](int, uint32_t key) {
       if (key > kNegInfKey && (key & mask) == prefix)
         atomicAdd(&sh.hist[(key >> shift) & 255u], 1u);
     });
@@ -338,13 +344,13 @@ __global__ void __launch_bounds__(kTopkThreads, 4)
 
   if (sh.finite <= static_cast<uint32_t>(k)) {
     // every finite value is selected
-    for_each_key<BF16_IN>(rp, N, [&](int j, uint32_t key) {
+    for_each_key<NT, BF16_IN>(rp, N, [&](int j, uint32_t key) {
       if (key > kNegInfKey) out[atomicAdd(&sh.out, 1u)] = j;
     });
   } else {
     // Sweep 3: columns above the boundary bin are in; the bin is compacted.
     const uint32_t hi16 = sh.prefix >> 16;
-    for_each_key<BF16_IN>(rp, N, [&](int j, uint32_t key) {
+    for_each_key<NT, BF16_IN>(rp, N, [&](int j, uint32_t key) {
       if (key <= kNegInfKey) return;
       const uint32_t top = key >> 16;
       if (top > hi16) {
@@ -363,15 +369,15 @@ __global__ void __launch_bounds__(kTopkThreads, 4)
     // The two low digits, from the compacted bin or by sweeps over the row.
     for (int pass = 2; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
-      topk_clear_hist(sh);
+      topk_clear_hist<NT>(sh);
       const uint32_t prefix = sh.prefix, mask = sh.mask;
       if (in_smem) {
-        for (uint32_t c = tid; c < nc; c += kTopkThreads) {
+        for (uint32_t c = tid; c < nc; c += NT) {
           const uint32_t key = sh.cand_key[c];
           if ((key & mask) == prefix) atomicAdd(&sh.hist[(key >> shift) & 255u], 1u);
         }
       } else {
-        for_each_key<BF16_IN>(rp, N, [&](int, uint32_t key) {
+        for_each_key<NT, BF16_IN>(rp, N, [&](int, uint32_t key) {
           if (key > kNegInfKey && (key & mask) == prefix)
             atomicAdd(&sh.hist[(key >> shift) & 255u], 1u);
         });
@@ -387,15 +393,15 @@ __global__ void __launch_bounds__(kTopkThreads, 4)
       if (t) out[atomicAdd(&sh.out, 1u)] = j;
     };
     if (in_smem) {
-      for (uint32_t c = tid; c < nc; c += kTopkThreads) take(sh.cand_idx[c], sh.cand_key[c]);
+      for (uint32_t c = tid; c < nc; c += NT) take(sh.cand_idx[c], sh.cand_key[c]);
     } else {
-      for_each_key<BF16_IN>(rp, N, [&](int j, uint32_t key) {
+      for_each_key<NT, BF16_IN>(rp, N, [&](int j, uint32_t key) {
         if (key > kNegInfKey) take(j, key);
       });
     }
   }
   __syncthreads();
-  for (int i = static_cast<int>(sh.out) + tid; i < k; i += kTopkThreads) out[i] = -1;
+  for (int i = static_cast<int>(sh.out) + tid; i < k; i += NT) out[i] = -1;
 }
 
 }  // namespace dsa
