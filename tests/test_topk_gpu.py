@@ -57,6 +57,22 @@ def test_topk_random_rows(N, k, dtype):
     check_topk(x.float().double().cpu().numpy(), sel.cpu().numpy(), k)
 
 
+@pytest.mark.parametrize("extra", [0, 1])
+def test_topk_both_block_sizes(extra):
+    """Calls with at most two rows per SM run 1024 threads per row, larger
+    ones 512: the rows on either side of that line give the same answers."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rows, N, k = 2 * sms + extra, 8192, 512
+    g = torch.Generator(device="cuda").manual_seed(7 + extra)
+    x = torch.randn(rows, N, device="cuda", generator=g)
+    lo = torch.randint(0, N, (rows, 1), device="cuda", generator=g)
+    cols = torch.arange(N, device="cuda")[None, :]
+    x = torch.where(cols >= lo // 2, x, torch.full_like(x, float("-inf")))
+    sel = binding.indexer_topk(x, k)
+    torch.cuda.synchronize()
+    check_topk(x.double().cpu().numpy(), sel.cpu().numpy(), k)
+
+
 def test_topk_strided_rows_and_prefix_columns():
     x = torch.randn(20, 1000, device="cuda")
     sel = binding.indexer_topk(x, 64, n=900)               # only the first 900 columns
