@@ -6,16 +6,32 @@ tcgen05 MMA, ReLU.w head reduction, masked store and -inf clean) over one
 synthetic workload resident in HBM. Prints ONE JSON line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME]
+                  [--workload NAME] [--split replicas|rows] [--zero-inputs]
+
+Default workload: MXFP8 S_q=8192, S_kv=65536 (the largest single-GPU
+configuration; DeepGEMM's MX logits numbers are quoted on this shape).
 
 Timing: W untimed warm-up calls; then K calls, each preceded by an untimed
 256 MiB write that flushes L2, each bracketed by CUDA events on the launch
 stream; barrier + synchronize around the timed region; max over ranks.
 `value` is in-window TFLOP/s = 2*H*D*(sum of window lengths) / time, for all
-ranks together. `e2e` repeats the measurement through the same public call
-with the inputs copied from pinned host memory and the logits copied back
-inside the timed region. `--impl reference` times the float64 CPU oracle on
-bounded row samples of the same workload.
+ranks together. `protocol` repeats the measurement the way DeepGEMM's MX
+reproducer times its kernel: each sample is 5 back-to-back calls into 5
+distinct output buffers between one pair of events (L2 flushed before the
+sample), 40 samples with the buffer order rotated, median/p10/p90 per call;
+`protocol_zero_inputs` does the same on all-zero Q/K/W with unit MX scales,
+the inputs DeepGEMM times. `e2e` measures the same call end to end from
+pinned host memory: inputs copied in and logits copied out inside the timed
+region, on three streams (copy in / compute / copy out) with two device
+buffer sets, so step i+1's inputs and step i-1's logits move while step i
+computes. `--impl reference` times the float64 CPU oracle on bounded row
+samples of the same workload.
+
+Multi-GPU (torchrun, one process per GPU): `--split replicas` (default) runs
+the whole workload on every rank (weak scaling); `--split rows` splits the
+query rows of ONE problem across the ranks, balanced by in-window work, each
+rank with the keys whole and its own output rows (strong scaling, no
+collective on the data path).
 """
 from __future__ import annotations
 
@@ -35,36 +51,27 @@ sys.path.insert(0, ROOT)
 
 METRIC = ("indexer logits µs/call and in-window TFLOP/s; "
           "% of GB300 dense tensor peak")
+DEFAULT_WORKLOAD = "mxfp8_8192x65536"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DTYPES = {0: "bf16", 1: "e4m3", 2: "mxfp8(e4m3+e8m0)", 3: "mxfp4(e2m1+e8m0)"}
 # dense tensor peak of a format relative to BF16 (nominal GB300 ratios)
 FMT_PEAK_RATIO = {0: 1.0, 1: 2.0, 2: 2.0, 3: 6.0}
 L2_FLUSH_BYTES = 256 << 20
-# DRAM bytes (read + write) of one kernel launch from an ncu capture, keyed by
-# workload, with the digest of the kernel sources it was taken on (see
-# profiles/). Reported as roofline.traffic only while the sources still match.
-PROFILED_TRAFFIC = {
-    "bf16_batched_causal_4096": ("a0ab85169a9d316f", 137.495040e6 + 79.709440e6),
-    "fp8_per_token_2048x32768": ("a0ab85169a9d316f", 21.721088e6 + 207.723008e6),
-    "mxfp8_2048x32768": ("a0ab85169a9d316f", 22.222592e6 + 207.570432e6),
-    "mxfp4_2048x32768": ("a0ab85169a9d316f", 11.900160e6 + 207.955968e6),
-    "paged_fp8_decode_64x2_32768": ("a0ab85169a9d316f", 208.284160e6 + 11.974400e6),
-    "mxfp8_8192x65536": ("a0ab85169a9d316f", 80375552 + 2087707904),
-    "mxfp4_8192x65536": ("a0ab85169a9d316f", 42581504 + 2087260416),
-    "mxfp4_irregular_8192x65536": ("a0ab85169a9d316f", 43101952 + 2086262272),
-    "thd_bf16_3seq_8192x32768": ("a0ab85169a9d316f", 145004800 + 1013174528),
-}
+# Files that define the logits kernel: a DRAM-traffic figure taken with ncu
+# (profiles/) is reported as roofline.traffic only while these still hash to
+# the digest it was taken on.
+KERNEL_FILES = ("indexer_kernel.cuh", "ptx.cuh", "plan_kernel.cuh")
+# DRAM bytes (read + write) of one logits-kernel launch from an ncu capture,
+# keyed by workload, with the kernel-source digest it was taken on.
+PROFILED_TRAFFIC = {}
 
 
 def kernel_source_digest() -> str:
-    """Digest of the sources that define and launch the logits kernel (the
-    top-k kernel's file is left out: it does not change the logits launch)."""
+    """Digest of the sources that define the logits kernel."""
     import hashlib
     d = os.path.join(ROOT, "infra_dsa_indexer_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(d)):
-        if f.startswith("topk"):
-            continue
+    for f in KERNEL_FILES:
         h.update(f.encode())
         with open(os.path.join(d, f), "rb") as fh:
             h.update(fh.read())
@@ -74,17 +81,23 @@ def kernel_source_digest() -> str:
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="bf16_batched_causal_4096")
-    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--split", choices=["replicas", "rows"], default="replicas",
+                    help="multi-GPU: whole problem per rank, or one problem's rows split")
+    ap.add_argument("--zero-inputs", action="store_true",
+                    help="time all-zero Q/K/W (unit MX scales) in the main measurement too")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--protocol-samples", type=int, default=40)
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="--impl reference: CPU seconds all its steps together aim for")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-protocol", action="store_true")
     ap.add_argument("--topk", type=int, default=0,
                     help="also time indexer_topk (k columns per row) on the call's logits")
     ap.add_argument("--out-bf16", action="store_true",
@@ -263,11 +276,15 @@ def run_reference(args, _dist):
         tot_t += dt
         tot_p += pr
     value = 2.0 * case.H * case.D * tot_p / tot_t / 1e12
-    sample = f"{nrows} uniformly drawn rows per step of {total_rows}"
+    sample = (f"{nrows} uniformly drawn rows per step of {total_rows}; ms_per_step is scaled "
+              f"to the whole workload by in-window pairs ({tot_p / args.steps:.0f} sampled "
+              f"of {int(pairs.sum())} per step)")
+    sample_ms = 1e3 * tot_t / args.steps
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True,
+        "ms_per_step": sample_ms * max(int(pairs.sum()), 1) / max(tot_p / args.steps, 1.0),
+        "sample_ms_per_step": sample_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(case, args),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nth, "kind": "oracle",
@@ -280,19 +297,39 @@ def run_reference(args, _dist):
 
 def workload_config(case, args):
     from infra_dsa_indexer_gb300 import synth
+    split = getattr(args, "split", "replicas")
     return {"workload": args.workload, "B": case.B, "S_q": case.S, "S_kv": case.N,
             "H": case.H, "D": case.D, "format": synth.FMT_NAMES[case.fmt],
             "w_format": "bf16" if case.w_fmt == synth.W_BF16 else "f32",
             "in_window_pairs": case.in_window_pairs(), "clean": bool(case.clean),
             "group_rows": bool(case.group_rows),
             "out_format": "bf16" if getattr(args, "out_bf16", False) else "f32",
+            "inputs": "all-zero (unit MX scales)" if getattr(args, "zero_inputs", False)
+                      else "seeded N(0,1), quantised",
             "l2": "flushed before every timed call (256 MiB write)",
-            "parallelism": f"replicas x{args.gpus}"}
+            "parallelism": (f"query-row split x{args.gpus}" if split == "rows"
+                            else f"replicas x{args.gpus}")}
+
+
+def zero_inputs_(t):
+    """All-zero Q/K/W with unit MX scales (E8M0 0x7f) and unit per-key FP8
+    scales, in place: the inputs DeepGEMM's reproducer times."""
+    for key in ("q", "k", "w"):
+        t[key].zero_()
+    for key in ("q_sf", "k_sf"):
+        if t.get(key) is not None:
+            t[key].fill_(0x7F)
+    if t.get("k_scales") is not None:
+        t["k_scales"].fill_(1.0)
+
+
+def _pct(sorted_vals, q):
+    return sorted_vals[int(q * (len(sorted_vals) - 1))]
 
 
 def run_ours(args, dist):
     import torch
-    from infra_dsa_indexer_gb300 import binding, synth
+    from infra_dsa_indexer_gb300 import binding, split, synth
     from infra_dsa_indexer_gb300 import build as lib_build
 
     dev = dist.local_rank
@@ -302,14 +339,49 @@ def run_ours(args, dist):
     dist.barrier()
     binding.load()
     case = synth.make_workload(args.workload)
-    flops = case.in_window_flops()
+    flops_total = case.in_window_flops()
     t = binding.case_to_device(case, device=f"cuda:{dev}", out_bf16=args.out_bf16)
+    if args.zero_inputs:
+        zero_inputs_(t)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=f"cuda:{dev}")
     launches_per_call = binding.indexer_launches_per_call(t["shape"])
 
+    # What this rank computes in one step: the whole problem (replicas), or
+    # its query rows of the one problem (rows; one B=1 call per batch slice).
+    if args.split == "rows" and dist.world > 1:
+        if case.page_size:
+            raise SystemExit("--split rows covers contiguous keys only")
+        mine = split.row_split(case.ks, case.ke, case.N, dist.world)[dist.rank]
+        views = []
+        for b, s0, s1 in mine:
+            v = split.slice_tensors(t, b, s0, s1)
+            v["shape"] = binding.make_shape(1, s1 - s0, case.N, case.H, case.D, case.fmt,
+                                            case.w_fmt, out_row_stride=t["shape"].out_row_stride,
+                                            flags=t["shape"].flags)
+            views.append(v)
+        lo = np.clip(case.ks.astype(np.int64), 0, case.N)
+        hi = np.clip(case.ke.astype(np.int64), 0, case.N)
+        pairs = np.maximum(hi - lo, 0)
+        my_pairs = sum(int(pairs[b, s0:s1].sum()) for b, s0, s1 in mine)
+        flops_rank = 2.0 * case.H * case.D * my_pairs
+        flops_all = flops_total                       # one problem, split
+        scaling = "strong"
+    else:
+        views = [t]
+        flops_rank = flops_total
+        flops_all = dist.world * flops_total          # one problem per rank
+        scaling = "weak"
+    calls_per_step = len(views)
+
+    def step(out=None, st=stream):
+        for v in views:
+            if out is not None:
+                v = dict(v, out=out)
+            binding.run_case(case, v, stream=st)
+
     for _ in range(args.warmup):
-        binding.run_case(case, t, stream=stream)
+        step()
     torch.cuda.synchronize()
     st = binding.indexer_get_last_error(stream)
     if st != binding.IDX_OK:
@@ -326,7 +398,7 @@ def run_ours(args, dist):
     for i in range(args.steps):
         flush.fill_(float(i))
         starts[i].record(stream)
-        binding.run_case(case, t, stream=stream)
+        step()
         ends[i].record(stream)
     torch.cuda.synchronize()
     dist.barrier()
@@ -335,14 +407,41 @@ def run_ours(args, dist):
     st = binding.indexer_get_last_error(stream)
     if st != binding.IDX_OK:
         raise RuntimeError(f"device error in timed region: {binding.indexer_status_string(st)}")
-    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]      # ms, one launch each
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]      # ms, one step each
     ms_local = sum(per) / len(per)
     ms = dist.max(ms_local, device=f"cuda:{dev}")
-    value = dist.world * flops / (ms * 1e-3) / 1e12
+    value = flops_all / (ms * 1e-3) / 1e12
+
+    # --- DeepGEMM-style protocol: 5 calls into 5 distinct outputs per sample
+    def protocol():
+        if args.no_protocol or len(views) != 1:
+            return None
+        outs = [t["out"]] + [torch.empty_like(t["out"]) for _ in range(4)]
+        for o in outs:
+            step(out=o)
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.protocol_samples)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.protocol_samples)]
+        torch.cuda.synchronize()
+        for smp in range(args.protocol_samples):
+            flush.fill_(float(smp))
+            e0[smp].record(stream)
+            for c in range(len(outs)):
+                step(out=outs[(smp + c) % len(outs)])
+            e1[smp].record(stream)
+        torch.cuda.synchronize()
+        us = sorted(1e3 * a.elapsed_time(b) / len(outs) for a, b in zip(e0, e1))
+        med = statistics.median(us)
+        del outs
+        return {"calls_per_sample": 5, "samples": args.protocol_samples,
+                "distinct_outputs": 5, "us_per_call_median": med,
+                "us_per_call_p10": _pct(us, 0.1), "us_per_call_p90": _pct(us, 0.9),
+                "tflops_median": flops_rank / (med * 1e-6) / 1e12}
+
+    prot = protocol()
 
     # --- top-k over the logits of the call (its own launches and events)
     topk = None
-    if args.topk:
+    if args.topk and len(views) == 1:
         idx = torch.empty(case.B, case.S, args.topk, dtype=torch.int32, device=f"cuda:{dev}")
         for _ in range(3):
             binding.indexer_topk(t["out"], args.topk, idx=idx, n=case.N, stream=stream)
@@ -362,32 +461,86 @@ def run_ours(args, dist):
                 "achieved_gbs": k_bytes / (k_ms * 1e-3) / 1e9, "gpu_launches": args.steps}
 
     # --- end to end through the same call: pinned host inputs in, logits out
-    e2e = None
-    if not args.no_e2e:
-        host = {}
-        for key in ("q", "k", "w", "ks", "ke", "q_sf", "k_sf", "k_scales", "block_table"):
-            if t.get(key) is not None:
-                host[key] = t[key].cpu().pin_memory()
-        out_host = torch.empty(t["out"].shape, dtype=t["out"].dtype).pin_memory()
+    def e2e(out_bf16):
+        """Three streams (copy in, compute, copy out) over two device buffer
+        sets: step i's call overlaps step i+1's input copy and step i-1's
+        logits copy. Timed from the first input copy to the last logits copy."""
+        keys = [key for key in ("q", "k", "w", "ks", "ke", "q_sf", "k_sf", "k_scales",
+                                "block_table") if t.get(key) is not None]
+        host = {key: t[key].cpu().pin_memory() for key in keys}
+        sets = []
+        for i in range(2):
+            d = dict(t)
+            for key in keys:
+                d[key] = t[key] if i == 0 else torch.empty_like(t[key])
+            d["out"] = torch.empty(t["out"].shape, device=t["out"].device,
+                                   dtype=torch.bfloat16 if out_bf16 else torch.float32)
+            d["shape"] = binding.make_shape(
+                case.B, case.S, case.N, case.H, case.D, case.fmt, case.w_fmt,
+                out_row_stride=t["shape"].out_row_stride,
+                flags=(t["shape"].flags & ~binding.IDX_FLAG_OUT_BF16) |
+                      (binding.IDX_FLAG_OUT_BF16 if out_bf16 else 0))
+            sets.append(d)
+        out_host = [torch.empty(sets[0]["out"].shape, dtype=sets[0]["out"].dtype).pin_memory()
+                    for _ in range(2)]
         h2d = sum(v.numel() * v.element_size() for v in host.values())
-        d2h = out_host.numel() * out_host.element_size()
-        n_e2e = max(3, min(args.e2e_steps, args.steps))
-        dist.barrier()
-        torch.cuda.synchronize()
+        d2h = out_host[0].numel() * out_host[0].element_size()
+        s_in, s_run, s_out = (torch.cuda.Stream() for _ in range(3))
+        n = max(3, min(args.e2e_steps, args.steps))
+        ev = lambda: torch.cuda.Event()
+        in_done = [ev() for _ in range(n)]
+        run_done = [ev() for _ in range(n)]
+        out_done = [ev() for _ in range(n)]
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(n_e2e):
-            for key, v in host.items():
-                t[key].copy_(v, non_blocking=True)
-            binding.run_case(case, t, stream=stream)
-            out_host.copy_(t["out"], non_blocking=True)
-        e1.record(stream)
+        dist.barrier()
         torch.cuda.synchronize()
-        e2e_ms = dist.max(e0.elapsed_time(e1) / n_e2e, device=f"cuda:{dev}")
-        e2e = {"value": dist.world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-               "ms_per_step": e2e_ms, "steps": n_e2e,
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+        e0.record(s_in)
+        for i in range(n):
+            d = sets[i % 2]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(run_done[i - 2])      # set's inputs no longer read
+                for key in keys:
+                    d[key].copy_(host[key], non_blocking=True)
+                in_done[i].record(s_in)
+            with torch.cuda.stream(s_run):
+                s_run.wait_event(in_done[i])
+                if i >= 2:
+                    s_run.wait_event(out_done[i - 2])     # set's logits copied out
+                binding.run_case(case, d, stream=s_run)
+                run_done[i].record(s_run)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(run_done[i])
+                out_host[i % 2].copy_(d["out"], non_blocking=True)
+                out_done[i].record(s_out)
+        e1.record(s_out)
+        torch.cuda.synchronize()
+        st_ = binding.indexer_get_last_error(s_run)
+        if st_ != binding.IDX_OK:
+            raise RuntimeError(f"device error in e2e: {binding.indexer_status_string(st_)}")
+        e2e_ms = dist.max(e0.elapsed_time(e1) / n, device=f"cuda:{dev}")
+        res = {"value": dist.world * flops_total / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": e2e_ms, "steps": n, "logits": "bf16" if out_bf16 else "f32",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "host_link_gbs": (h2d + d2h) / (e2e_ms * 1e-3) / 1e9,
+               "pipeline": "3 streams (copy in / compute / copy out), 2 buffer sets"}
+        del sets, out_host, host
+        torch.cuda.empty_cache()
+        return res
+
+    e2e_main = e2e_bf16 = None
+    if not args.no_e2e and len(views) == 1:
+        e2e_main = e2e(args.out_bf16)
+        if not args.out_bf16:
+            e2e_bf16 = e2e(True)
+
+    # --- the protocol again on all-zero inputs (unit MX scales)
+    prot_zero = None
+    if not args.zero_inputs and prot is not None:
+        zero_inputs_(t)
+        torch.cuda.synchronize()
+        prot_zero = protocol()
 
     if dist.rank != 0:
         return
@@ -396,18 +549,19 @@ def run_ours(args, dist):
         topk["peak_gbs"] = peaks["hbm_gbs"]
         topk["frac"] = topk["achieved_gbs"] / peaks["hbm_gbs"]
     peak = peaks["bf16_tflops"] * FMT_PEAK_RATIO[case.fmt]
-    achieved = flops / (ms_local * 1e-3) / 1e12
+    achieved = flops_rank / (ms_local * 1e-3) / 1e12
     srt = sorted(per)
-    prof = None if args.out_bf16 else PROFILED_TRAFFIC.get(args.workload)
+    prof = None if (args.out_bf16 or len(views) != 1) else PROFILED_TRAFFIC.get(args.workload)
     traffic = prof[1] if prof and prof[0] == kernel_source_digest() else None
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": achieved / peak, "traffic": traffic,
             "peak_source": (f"{peak_src} bf16 burst x{FMT_PEAK_RATIO[case.fmt]:g} "
                             "(nominal format ratio)" if case.fmt else f"{peak_src} bf16 burst"),
             "kernel": "dsa::indexer_logits_kernel",
-            "algorithmic_flops_per_launch": flops,
+            "kernel_source_digest": kernel_source_digest(),
+            "algorithmic_flops_per_launch": flops_rank / calls_per_step,
             "hbm_write_gbs": case.B * case.S * case.N * (2 if args.out_bf16 else 4)
-                             / (ms_local * 1e-3) / 1e9,
+                             / (ms_local * 1e-3) / 1e9 * (flops_rank / flops_total),
             "hbm_peak_gbs": peaks["hbm_gbs"]}
     if case.page_size:
         # Decode reads each batch's keys once and is bound by HBM: report
@@ -431,14 +585,17 @@ def run_ours(args, dist):
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": dist.world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-        "us_per_call": 1e3 * ms, "us_per_call_median": 1e3 * statistics.median(per),
-        "us_per_call_p10": 1e3 * srt[int(0.1 * (len(srt) - 1))],
-        "us_per_call_p90": 1e3 * srt[int(0.9 * (len(srt) - 1))],
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": DTYPES[case.fmt], "data": "synthetic (seeded N(0,1) inputs, quantised)",
+        "us_per_call": 1e3 * ms / calls_per_step,
+        "us_per_call_median": 1e3 * statistics.median(per) / calls_per_step,
+        "us_per_call_p10": 1e3 * _pct(srt, 0.1) / calls_per_step,
+        "us_per_call_p90": 1e3 * _pct(srt, 0.9) / calls_per_step,
+        "higher_is_better": True, "scaling": scaling, "vs_baseline": None,
+        "dtype": DTYPES[case.fmt], "data": "synthetic (seeded N(0,1) inputs, quantised)"
+        if not args.zero_inputs else "synthetic (all-zero inputs, unit MX scales)",
         "config": workload_config(case, args),
-        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "topk": topk,
-        "gpu_launches": args.steps * launches_per_call,
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e_main, "e2e_bf16_logits": e2e_bf16,
+        "protocol": prot, "protocol_zero_inputs": prot_zero, "topk": topk,
+        "gpu_launches": args.steps * launches_per_call * calls_per_step,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

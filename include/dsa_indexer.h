@@ -140,9 +140,11 @@ typedef struct idx_shape {
  * the host before any launch. A device-side wait that runs out is reported
  * by indexer_get_last_error(), not here. The first call on a (device,
  * stream) pair allocates a small library-owned scratch block (a work counter
- * and an error word, plus B*S words for IDX_FLAG_GROUP_ROWS; a later call that
- * needs more frees and re-allocates it, waiting for the device), so make one
- * call of the largest shape before capturing a CUDA graph on that stream;
+ * and an error word, plus B*S words for IDX_FLAG_GROUP_ROWS) from the device's
+ * stream-ordered pool; a later call that needs more grows it on `stream`
+ * (cudaMallocAsync / cudaFreeAsync, no synchronisation). Make one call of the
+ * largest shape before capturing a CUDA graph on that stream, and release a
+ * short-lived stream's block with indexer_stream_release;
  * calls on one stream reuse it, so calls on the same stream must not overlap
  * (stream order guarantees that).
  */
@@ -168,8 +170,10 @@ IDX_API int indexer_logits(const void* q, const uint8_t* q_sf, const void* k, co
  * kernel, because the array keeps the previous call's contents. All calls on
  * a device share the one array, so calls that can overlap on the GPU (on
  * different streams without ordering) race and must not be issued that way.
- * A device-side wait that runs out is recorded only in that shared array;
- * indexer_get_last_error does not report it for this entry point. */
+ * A device-side wait that runs out is recorded in that shared array, not in
+ * the per-stream word indexer_get_last_error reads: read it with
+ * indexer_noalloc_get_last_error after the call and before the next
+ * no-allocation call on the device (which clears it). */
 IDX_API int indexer_logits_noalloc(const void* q, const uint8_t* q_sf, const void* k,
                                    const uint8_t* k_sf, const float* k_scales, const void* w,
                                    const int32_t* ks, const int32_t* ke, float sm_scale,
@@ -241,6 +245,23 @@ IDX_API const char* indexer_status_string(int status);
  * call was ever made on the pair, IDX_ERR_CUDA if synchronisation fails. */
 IDX_API int indexer_get_last_error(idx_stream_t stream);
 
+/* indexer_get_last_error for indexer_logits_noalloc: synchronise `stream`,
+ * then return and clear the error word of the current device's fixed
+ * no-allocation array (IDX_OK, or IDX_ERR_TIMEOUT if the last no-allocation
+ * call on the device gave up waiting; its output is then invalid). Call it
+ * before the next no-allocation call on the device, which clears the word.
+ * Allocates nothing. Returns IDX_OK when no no-allocation call was ever made
+ * on the device, IDX_ERR_CUDA if synchronisation fails. */
+IDX_API int indexer_noalloc_get_last_error(idx_stream_t stream);
+
+/* Free the library scratch block of the (current device, stream) pair, if
+ * any, stream-ordered on `stream` (no synchronisation). A caller that makes
+ * calls on short-lived streams calls this after its last call on a stream and
+ * before destroying it; otherwise each such stream keeps its block (256 bytes,
+ * plus B*S words after grouped calls) until indexer_shutdown. A later call on
+ * the pair allocates again. Returns IDX_OK or IDX_ERR_CUDA. */
+IDX_API int indexer_stream_release(idx_stream_t stream);
+
 /* Device-side wait limit in nanoseconds for later launches from this process
  * (default 2e9). Used by tests to make a wait run out on purpose; values
  * below 1e6 are raised to 1e6. Returns the previous value. */
@@ -256,6 +277,13 @@ IDX_API int64_t indexer_set_wait_limit_ns(int64_t ns);
  * stays usable. Returns IDX_OK once enqueued, IDX_ERR_DEVICE off sm_103,
  * IDX_ERR_CUDA if allocation or launch fails. */
 IDX_API int indexer_selftest_wait_timeout(int64_t limit_ns, idx_stream_t stream);
+
+/* The failure-detection self-test above, aimed at the fixed array of
+ * indexer_logits_noalloc instead of a per-stream word (no counterpart in the
+ * method; allocates nothing): indexer_noalloc_get_last_error then returns
+ * IDX_ERR_TIMEOUT once and clears it. Same limits and returns as
+ * indexer_selftest_wait_timeout. */
+IDX_API int indexer_noalloc_selftest_wait_timeout(int64_t limit_ns, idx_stream_t stream);
 
 /* Number of kernel launches one indexer_logits call with this shape makes
  * (2 with IDX_FLAG_GROUP_ROWS in effect, else 1); for launch counts in

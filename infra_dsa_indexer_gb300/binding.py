@@ -82,6 +82,12 @@ def load():
         lib.indexer_topk.argtypes = [vp, i32, i64, i32, i64, i32, vp, i64, vp]
         lib.indexer_selftest_wait_timeout.restype = i32
         lib.indexer_selftest_wait_timeout.argtypes = [i64, vp]
+        lib.indexer_noalloc_get_last_error.restype = i32
+        lib.indexer_noalloc_get_last_error.argtypes = [vp]
+        lib.indexer_noalloc_selftest_wait_timeout.restype = i32
+        lib.indexer_noalloc_selftest_wait_timeout.argtypes = [i64, vp]
+        lib.indexer_stream_release.restype = i32
+        lib.indexer_stream_release.argtypes = [vp]
         lib.indexer_launches_per_call.restype = i32
         lib.indexer_launches_per_call.argtypes = [ctypes.POINTER(idx_shape)]
         lib.indexer_shutdown.restype = i32
@@ -203,6 +209,20 @@ def indexer_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
     st = load().indexer_selftest_wait_timeout(int(limit_ns), _stream(stream))
     if st != IDX_OK:
         raise IndexerError(st, "indexer_selftest_wait_timeout")
+
+
+def indexer_noalloc_get_last_error(stream=None) -> int:
+    return load().indexer_noalloc_get_last_error(_stream(stream))
+
+
+def indexer_noalloc_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    st = load().indexer_noalloc_selftest_wait_timeout(int(limit_ns), _stream(stream))
+    if st != IDX_OK:
+        raise IndexerError(st, "indexer_noalloc_selftest_wait_timeout")
+
+
+def indexer_stream_release(stream=None) -> int:
+    return load().indexer_stream_release(_stream(stream))
 
 
 def indexer_launches_per_call(shape: idx_shape) -> int:

@@ -71,8 +71,12 @@ int get_encoder() {
   return IDX_OK;
 }
 
-// At least `words` words of scratch for (dev, stream). Growing frees the old
-// block (cudaFree waits for the device) and carries the error word over.
+// At least `words` words of scratch for (dev, stream), stream-ordered: the
+// block comes from the device's stream-ordered pool (cudaMallocAsync), so
+// neither the first allocation nor a later growth waits for the device.
+// Growing allocates the larger block on `stream`, carries the error word over
+// with a device-to-device copy on `stream` and frees the old block on
+// `stream` (after every earlier call on it has finished with it).
 int get_scratch(int dev, cudaStream_t stream, int64_t words, int32_t** out) {
   words = std::max<int64_t>(words, kScratchInts);
   Scratch& sc = g_scratch[std::make_pair(dev, reinterpret_cast<uintptr_t>(stream))];
@@ -80,20 +84,15 @@ int get_scratch(int dev, cudaStream_t stream, int64_t words, int32_t** out) {
     *out = sc.ptr;
     return IDX_OK;
   }
-  int32_t err = 0;
-  if (sc.ptr != nullptr) {
-    if (cudaDeviceSynchronize() != cudaSuccess ||
-        cudaMemcpy(&err, sc.ptr + 2, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess ||
-        cudaFree(sc.ptr) != cudaSuccess)
-      return IDX_ERR_CUDA;
-    sc.ptr = nullptr;
-    sc.words = 0;
-  }
-  int32_t* p = nullptr;
-  if (cudaMalloc(&p, words * sizeof(int32_t)) != cudaSuccess) return IDX_ERR_CUDA;
-  if (cudaMemset(p, 0, kScratchInts * sizeof(int32_t)) != cudaSuccess ||
-      (err != 0 && cudaMemcpy(p + 2, &err, sizeof(err), cudaMemcpyHostToDevice) != cudaSuccess)) {
-    cudaFree(p);
+  void* raw = nullptr;
+  if (cudaMallocAsync(&raw, words * sizeof(int32_t), stream) != cudaSuccess) return IDX_ERR_CUDA;
+  int32_t* p = static_cast<int32_t*>(raw);
+  if (cudaMemsetAsync(p, 0, kScratchInts * sizeof(int32_t), stream) != cudaSuccess ||
+      (sc.ptr != nullptr &&
+       (cudaMemcpyAsync(p + 2, sc.ptr + 2, sizeof(int32_t), cudaMemcpyDeviceToDevice, stream) !=
+            cudaSuccess ||
+        cudaFreeAsync(sc.ptr, stream) != cudaSuccess))) {
+    cudaFreeAsync(p, stream);
     return IDX_ERR_CUDA;
   }
   sc.ptr = p;
@@ -189,7 +188,7 @@ int launch(const KernelParams& prm, int grid, DeviceInfo* di, cudaStream_t strea
 
 extern "C" {
 
-int indexer_version(void) { return 100; }
+int indexer_version(void) { return 200; }
 
 int indexer_launches_per_call(const idx_shape* shape) {
   return shape != nullptr && groups_rows(*shape, false) ? 2 : 1;
@@ -437,6 +436,42 @@ int indexer_get_last_error(idx_stream_t stream_) {
   return word == 0 ? IDX_OK : (word == dsa::kErrTimeout ? IDX_ERR_TIMEOUT : word);
 }
 
+int indexer_noalloc_get_last_error(idx_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return IDX_ERR_CUDA;
+  int32_t* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (dev < 0 || dev >= kMaxDevices || g_fixed_scratch_addr[dev] == nullptr) return IDX_OK;
+    scratch = g_fixed_scratch_addr[dev];
+  }
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return IDX_ERR_CUDA;
+  int32_t word = 0;
+  if (cudaMemcpy(&word, scratch + 2, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return IDX_ERR_CUDA;
+  if (word != 0) {
+    const int32_t zero[kScratchWordsPerCall] = {0, 0, 0};
+    if (cudaMemcpy(scratch, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return IDX_ERR_CUDA;
+  }
+  return word == 0 ? IDX_OK : (word == dsa::kErrTimeout ? IDX_ERR_TIMEOUT : word);
+}
+
+int indexer_stream_release(idx_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return IDX_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  auto it = g_scratch.find(std::make_pair(dev, reinterpret_cast<uintptr_t>(stream)));
+  if (it == g_scratch.end()) return IDX_OK;
+  const int rc = it->second.ptr == nullptr || cudaFreeAsync(it->second.ptr, stream) == cudaSuccess
+                     ? IDX_OK
+                     : IDX_ERR_CUDA;
+  g_scratch.erase(it);
+  return rc;
+}
+
 int indexer_topk(const void* logits, int logits_bf16, int64_t rows, int32_t N,
                  int64_t row_stride, int32_t k, int32_t* idx, int64_t idx_stride,
                  idx_stream_t stream_) {
@@ -494,6 +529,24 @@ int indexer_selftest_wait_timeout(int64_t limit_ns, idx_stream_t stream_) {
     if (st) return st;
     if (di->cc_major != 10 || di->cc_minor != 3) return IDX_ERR_DEVICE;
     if ((st = get_scratch(dev, stream, kScratchInts, &scratch))) return st;
+  }
+  dsa::wait_selftest_kernel<<<1, 32, 0, stream>>>(scratch, static_cast<uint64_t>(limit_ns));
+  return cudaGetLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+}
+
+int indexer_noalloc_selftest_wait_timeout(int64_t limit_ns, idx_stream_t stream_) {
+  if (limit_ns < 1000 || limit_ns > 1000000000LL) return IDX_ERR_SHAPE;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return IDX_ERR_CUDA;
+  int32_t* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo* di = nullptr;
+    int st = get_device_info(dev, &di);
+    if (st) return st;
+    if (di->cc_major != 10 || di->cc_minor != 3) return IDX_ERR_DEVICE;
+    if ((st = get_fixed_scratch(dev, &scratch))) return st;
   }
   dsa::wait_selftest_kernel<<<1, 32, 0, stream>>>(scratch, static_cast<uint64_t>(limit_ns));
   return cudaGetLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;

@@ -2,7 +2,9 @@
 
 The bar: the -inf pattern is bit-exact on every compared row, every in-window
 value is finite, and in-window |gpu - ref| / (1e-6 + den) <= 2e-3 where
-den = sum_h |w_h| * |sm_scale * q_h . k| (the oracle's float64 value).
+den = sum_h |w_h| * |sm_scale * q_h . k| (the oracle's float64 value). The
+error is also logged against the looser scale
+den_abs = sum_h |w_h| * |sm_scale| * sum_d |q_hd| * |k_d| when it is given.
 """
 import numpy as np
 
@@ -11,12 +13,15 @@ import oracle
 REL_TOL = 2e-3
 
 
-def oracle_rows(case, rows=None, nthreads=0):
-    out, den, _ = oracle.logits(case.fmt, case.q, case.k, case.w, case.ks, case.ke,
-                                case.sm_scale, q_sf=case.q_sf, k_sf=case.k_sf,
-                                k_tok=case.k_tok, w_fmt=case.w_fmt, H=case.H, D=case.D,
-                                rows=rows, nthreads=nthreads)
-    return out, den
+def oracle_rows(case, rows=None, nthreads=0, want_den_abs=False):
+    """(out, den) of the oracle, float64 [R, N]; with want_den_abs also the
+    looser scale sum_h |w_h| |sm_scale| sum_d |q_hd| |k_d| as a third item."""
+    out, den, den_abs = oracle.logits(case.fmt, case.q, case.k, case.w, case.ks, case.ke,
+                                      case.sm_scale, q_sf=case.q_sf, k_sf=case.k_sf,
+                                      k_tok=case.k_tok, w_fmt=case.w_fmt, H=case.H, D=case.D,
+                                      rows=rows, nthreads=nthreads,
+                                      want_den_abs=want_den_abs)
+    return (out, den, den_abs) if want_den_abs else (out, den)
 
 
 def expected_mask(case, rows=None):
@@ -31,7 +36,13 @@ def expected_mask(case, rows=None):
     return (cols < lo) | (cols >= hi)
 
 
-def compare(gpu_rows, ref, den, *, check_outside=True, tol=REL_TOL, out_rounding=0.0):
+# (label, worst error over den, worst error over den_abs) of every compare()
+# given den_abs; printed as it goes (pytest -s shows it).
+LOG = []
+
+
+def compare(gpu_rows, ref, den, *, check_outside=True, tol=REL_TOL, out_rounding=0.0,
+            den_abs=None, label=""):
     """gpu_rows, ref, den: [R, N]. Returns the max relative error in-window.
 
     out_rounding: relative rounding bound of a narrower output format, added
@@ -49,5 +60,11 @@ def compare(gpu_rows, ref, den, *, check_outside=True, tol=REL_TOL, out_rounding
     rel = np.maximum(np.abs(g - ref[inside]) - out_rounding * np.abs(ref[inside]), 0.0) / (
         1e-6 + den[inside])
     worst = float(rel.max()) if rel.size else 0.0
+    if den_abs is not None:
+        rel_abs = np.maximum(np.abs(g - ref[inside]) - out_rounding * np.abs(ref[inside]),
+                             0.0) / (1e-6 + den_abs[inside])
+        worst_abs = float(rel_abs.max()) if rel_abs.size else 0.0
+        LOG.append((label, worst, worst_abs))
+        print(f"parity {label}: max err / den {worst:.3e}, / den_abs {worst_abs:.3e}")
     assert worst <= tol, f"max relative error {worst:.3e} > {tol}"
     return worst

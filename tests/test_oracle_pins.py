@@ -112,12 +112,16 @@ def library_route(case):
     x = case.sm_scale * dots
     out = np.einsum("bsh,bshn->bsn", w, np.maximum(x, 0.0))
     den = np.einsum("bsh,bshn->bsn", np.abs(w), np.abs(x))
+    # the looser scale: sum_h |w_h| |sm_scale| sum_d |q_hd| |k_d|
+    den_abs = abs(case.sm_scale) * np.einsum(
+        "bsh,bshn->bsn", np.abs(w), np.einsum("bshd,bnd->bshn", np.abs(qd), np.abs(kd)))
     cols = np.arange(case.N)
     lo = np.clip(case.ks, 0, case.N)[..., None]
     hi = np.clip(case.ke, 0, case.N)[..., None]
     inside = (cols >= lo) & (cols < hi)
     out = np.where(inside, out, -np.inf)
-    return out.reshape(-1, case.N), np.where(inside, den, 0).reshape(-1, case.N)
+    return (out.reshape(-1, case.N), np.where(inside, den, 0).reshape(-1, case.N),
+            np.where(inside, den_abs, 0).reshape(-1, case.N))
 
 
 @pytest.mark.parametrize("fmt", FMTS)
@@ -130,12 +134,16 @@ def test_library_route_agrees(fmt, w_fmt):
     ke = ks + rng.integers(-2, N, size=(B, S))
     case = synth.make_case(fmt, B, S, N, H=H, D=128, seed=11 + fmt, ks=ks, ke=ke,
                            w_fmt=w_fmt, sm_scale=0.37)
-    out, den, _ = run(case)
-    ref, rden = library_route(case)
+    out, den, den_abs = run(case, want_den_abs=True)
+    ref, rden, rden_abs = library_route(case)
     assert np.array_equal(np.isneginf(out), np.isneginf(ref))
     fin = np.isfinite(ref)
     assert np.all(np.abs(out[fin] - ref[fin]) <= 1e-12 * (1e-300 + rden[fin]) + 1e-300)
     assert np.allclose(den[fin], rden[fin], rtol=1e-12, atol=0)
+    assert np.allclose(den_abs[fin], rden_abs[fin], rtol=1e-12, atol=0)
+    assert np.all(den_abs[~fin] == 0) and np.all(den[~fin] == 0)
+    # |sum_d q k| <= sum_d |q||k| head by head, so den <= den_abs
+    assert np.all(den[fin] <= den_abs[fin] * (1 + 1e-12))
 
 
 # ---------------------------------------------------------------------------

@@ -38,7 +38,7 @@ def check_topk(vals, sel, k):
 
 
 @pytest.mark.parametrize("N,k", [(1, 1), (100, 7), (100, 150), (5000, 2048), (65536, 2048),
-                                 (3000, 2999)])
+                                 (3000, 2999), (65536, 4096), (8192, 5000)])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_topk_random_rows(N, k, dtype):
     g = torch.Generator(device="cuda").manual_seed(N + k)
@@ -73,6 +73,23 @@ def test_topk_both_block_sizes(extra):
     check_topk(x.double().cpu().numpy(), sel.cpu().numpy(), k)
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("N,k", [(65536, 20000), (65536, 2048), (9000, 4500)])
+def test_topk_tied_runs_overflow_the_boundary_bin(N, k, dtype):
+    """A few distinct values only, with k falling inside a run of equal values
+    far larger than the shared-memory candidate buffer: the boundary bin does
+    not fit, so the low digits are resolved by sweeps over the row."""
+    g = torch.Generator(device="cuda").manual_seed(N ^ k)
+    rows = 9
+    x = torch.randint(0, 4, (rows, N), device="cuda", generator=g).float() - 1.5
+    x[1, : N // 3] = float("-inf")             # a tied row with a prefix outside the window
+    x[2] = 0.25                                # one value only
+    x = x.to(dtype)
+    sel = binding.indexer_topk(x, k)
+    torch.cuda.synchronize()
+    check_topk(x.double().cpu().numpy(), sel.cpu().numpy(), k)
+
+
 def test_topk_strided_rows_and_prefix_columns():
     x = torch.randn(20, 1000, device="cuda")
     sel = binding.indexer_topk(x, 64, n=900)               # only the first 900 columns
@@ -101,6 +118,10 @@ def test_topk_of_indexer_logits_against_oracle(fmt):
         thr = np.sort(ref[r, finite])[::-1][k - 1]
         slack = REL_TOL * (1e-6 + den[r, picked]) * 2
         assert np.all(ref[r, picked] >= thr - slack), f"row {r}"
+        # and from above: a column whose oracle value beats the threshold by
+        # more than twice the logits tolerance was picked
+        sure = finite[ref[r, finite] > thr + 2 * REL_TOL * (1e-6 + den[r, finite])]
+        assert set(sure.tolist()) <= set(picked.tolist()), f"row {r}: missed a clear top-k column"
 
 
 def test_topk_full_size_mxfp8():
