@@ -750,10 +750,12 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
           }
           tc_cp_32x128b_warpx4(sfa, sfa_desc0 + ((st * kSfaBytes) >> 4));
         }
-        // With a single accumulator its release is on the critical path:
-        // poll for it rather than sleep.
-        if (!(kAccBufs > 1 ? mbar_wait(&acc_empty[acc], apar, abort_flag, p.timeout_ns)
-                           : mbar_wait_poll(&acc_empty[acc], apar, abort_flag, p.timeout_ns))) {
+        // Sleep until the accumulator is handed back, also with a single
+        // accumulator, where the wait is on the critical path: a polling
+        // thread takes issue slots from the epilogue warps on its scheduler,
+        // whose arithmetic is the longer part of the chain (measured: a
+        // polling wait made the MXFP8 kernel 5% slower).
+        if (!mbar_wait(&acc_empty[acc], apar, abort_flag, p.timeout_ns)) {
           ok = false;
           break;
         }

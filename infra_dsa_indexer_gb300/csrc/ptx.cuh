@@ -110,22 +110,6 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity,
   return false;
 }
 
-// Same contract, polling back to back: for a wait on the critical path, where
-// the wake-up delay of a suspended thread would show. The clock is read only
-// after the first few thousand polls.
-__device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity,
-                                               volatile int* abort, uint64_t timeout_ns) {
-  for (int i = 0; i < 4096; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t start = globaltimer_ns();
-  while (true) {
-    for (int i = 0; i < 256; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (globaltimer_ns() - start > timeout_ns) return false;
-  }
-}
-
 // ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor), completion counted in bytes on an mbarrier
 // ---------------------------------------------------------------------------
