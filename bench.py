@@ -100,6 +100,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-protocol", action="store_true")
     ap.add_argument("--topk", type=int, default=0,
                     help="also time indexer_topk (k columns per row) on the call's logits")
+    ap.add_argument("--fused-topk", type=int, default=0,
+                    help="also time indexer_logits_topk (k columns per row, no logits written) "
+                         "against indexer_logits + indexer_topk")
     ap.add_argument("--out-bf16", action="store_true",
                     help="write the logits as BF16 (IDX_FLAG_OUT_BF16) instead of FP32")
     return ap.parse_args(argv)
@@ -460,6 +463,50 @@ def run_ours(args, dist):
                 "bound": "hbm", "algorithmic_bytes_per_launch": k_bytes,
                 "achieved_gbs": k_bytes / (k_ms * 1e-3) / 1e9, "gpu_launches": args.steps}
 
+    # --- the fused call (logits never written) against logits + top-k
+    fused = None
+    if args.fused_topk and len(views) == 1 and not case.page_size and not args.out_bf16:
+        kf = args.fused_topk
+        shape_f = binding.make_shape(case.B, case.S, case.N, case.H, case.D, case.fmt,
+                                     case.w_fmt,
+                                     flags=binding.IDX_FLAG_GROUP_ROWS if case.group_rows else 0)
+        ws = torch.empty(binding.indexer_logits_topk_workspace_bytes(shape_f), dtype=torch.uint8,
+                         device=f"cuda:{dev}")
+        idx_f = torch.empty(case.B * case.S, kf, dtype=torch.int32, device=f"cuda:{dev}")
+        idx_s = torch.empty(case.B * case.S, kf, dtype=torch.int32, device=f"cuda:{dev}")
+
+        def fused_call():
+            binding.topk_case(case, t, kf, idx=idx_f, workspace=ws, stream=stream)
+
+        def separate_call():
+            step()
+            binding.indexer_topk(t["out"], kf, idx=idx_s.view(case.B, case.S, kf), n=case.N,
+                                 stream=stream)
+
+        res = {}
+        for name, fn in (("fused", fused_call), ("logits_then_topk", separate_call)):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+            for i in range(args.steps):
+                flush.fill_(float(i))
+                ev[i][0].record(stream)
+                fn()
+                ev[i][1].record(stream)
+            torch.cuda.synchronize()
+            res[name] = statistics.median(1e3 * a.elapsed_time(b) for a, b in ev)
+        st_ = binding.indexer_get_last_error(stream)
+        if st_ != binding.IDX_OK:
+            raise RuntimeError(f"device error in fused top-k: {binding.indexer_status_string(st_)}")
+        fused = {"k": kf, "us_per_call_fused": res["fused"],
+                 "us_per_call_logits_then_topk": res["logits_then_topk"],
+                 "speedup": res["logits_then_topk"] / res["fused"],
+                 "workspace_bytes": int(ws.numel()),
+                 "launches_fused": 5 + (1 if case.group_rows else 0)}
+        del ws
+
     # --- end to end through the same call: pinned host inputs in, logits out
     def e2e(out_bf16):
         """Three streams (copy in, compute, copy out) over two device buffer
@@ -595,6 +642,7 @@ def run_ours(args, dist):
         "config": workload_config(case, args),
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e_main, "e2e_bf16_logits": e2e_bf16,
         "protocol": prot, "protocol_zero_inputs": prot_zero, "topk": topk,
+        "fused_topk": fused,
         "gpu_launches": args.steps * launches_per_call * calls_per_step,
         "clocks": clk,
     }

@@ -71,7 +71,8 @@ typedef enum idx_status {
   IDX_ERR_CUDA = 7,        /* a CUDA runtime call failed (launch, allocation, ...)   */
   IDX_ERR_TIMEOUT = 8,     /* device-side wait gave up; the call's output is invalid */
   IDX_ERR_UNSUPPORTED = 9, /* valid request this build does not implement            */
-  IDX_ERR_SCRATCH = 10     /* indexer_logits_noalloc: more scratch than its array   */
+  IDX_ERR_SCRATCH = 10     /* indexer_logits_noalloc: more scratch than its array;
+                              indexer_logits_topk: workspace too small               */
 } idx_status;
 
 /* idx_shape.flags: the rows' windows are irregular (not a causal staircase);
@@ -235,6 +236,49 @@ IDX_API int indexer_paged_logits(const void* q, const uint8_t* q_sf, const void*
 IDX_API int indexer_topk(const void* logits, int logits_bf16, int64_t rows, int32_t N,
                          int64_t row_stride, int32_t k, int32_t* idx, int64_t idx_stride,
                          idx_stream_t stream);
+
+/* Bytes of device workspace indexer_logits_topk needs for this shape (any
+ * top-k size), or -1 for a NULL or invalid shape: about 4.1 * B*S*N bytes
+ * (as much as the FP32 logits would take), i.e. per row 4 bytes for each key
+ * (the sampled logits of one 128-key tile in four, a value slot for each key
+ * of the other tiles, so that no input can overflow it) and a mask word per
+ * 32 keys of the other tiles. Only kept values are written to the slots. */
+IDX_API int64_t indexer_logits_topk_workspace_bytes(const idx_shape* shape);
+
+/* The indexer's logits reduced straight to each row's top-k key columns, the
+ * way DeepSeek Sparse Attention consumes them (the FlashInfer page's sparse
+ * MLA prefill takes top-k = 2048 indices per query), without writing the
+ * B*S*N logits. Same inputs, checks and windows as indexer_logits (shape
+ * flags: IDX_FLAG_GROUP_ROWS only; clean is implied), and the same result as
+ * indexer_topk over indexer_logits' FP32 output: for every row the columns of
+ * its `topk` largest in-window logits, in no particular order, -1 padding
+ * when the window holds fewer; among values equal to the topk-th largest any
+ * subset of the right size. The logits are computed exactly as
+ * indexer_logits computes them.
+ *
+ * How: a first pass computes the logits of every fourth 128-key tile into
+ * the workspace; the topk-th largest of them is a lower bound T of the row's
+ * topk-th largest logit (those topk values are logits of the row); a second
+ * pass over the other tiles keeps only in-window logits >= T (at their own
+ * slots in the workspace, with a bit mask per 32 keys); a last selection
+ * takes the top-k of the sampled logits and the kept values. Five launches on `stream` (six with
+ * IDX_FLAG_GROUP_ROWS), no synchronisation, no host read of device data.
+ *
+ *  topk       >= 1.
+ *  idx        device, int32 [B*S, idx_stride], idx_stride >= topk; row b*S+i
+ *             gets its columns in [0, topk).
+ *  workspace  device, 256-byte aligned, at least
+ *             indexer_logits_topk_workspace_bytes(shape) bytes, owned by the
+ *             caller; its contents are scratch (not kept between calls).
+ * Returns IDX_ERR_SCRATCH if workspace_bytes is too small,
+ * IDX_ERR_UNSUPPORTED for IDX_FLAG_OUT_BF16, otherwise as indexer_logits.
+ * Contiguous keys only (no paged variant). */
+IDX_API int indexer_logits_topk(const void* q, const uint8_t* q_sf, const void* k,
+                                const uint8_t* k_sf, const float* k_scales, const void* w,
+                                const int32_t* ks, const int32_t* ke, float sm_scale,
+                                const idx_shape* shape, int32_t topk, int32_t* idx,
+                                int64_t idx_stride, void* workspace, int64_t workspace_bytes,
+                                idx_stream_t stream);
 
 /* Human-readable text for an idx_status value (static storage, never NULL). */
 IDX_API const char* indexer_status_string(int status);

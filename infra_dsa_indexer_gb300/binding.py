@@ -80,6 +80,11 @@ def load():
             ctypes.POINTER(idx_paged), vp]
         lib.indexer_topk.restype = i32
         lib.indexer_topk.argtypes = [vp, i32, i64, i32, i64, i32, vp, i64, vp]
+        lib.indexer_logits_topk_workspace_bytes.restype = i64
+        lib.indexer_logits_topk_workspace_bytes.argtypes = [ctypes.POINTER(idx_shape)]
+        lib.indexer_logits_topk.restype = i32
+        lib.indexer_logits_topk.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float,
+                                            ctypes.POINTER(idx_shape), i32, vp, i64, vp, i64, vp]
         lib.indexer_selftest_wait_timeout.restype = i32
         lib.indexer_selftest_wait_timeout.argtypes = [i64, vp]
         lib.indexer_noalloc_get_last_error.restype = i32
@@ -202,6 +207,43 @@ def indexer_topk(logits, k: int, idx=None, n=None, stream=None):
                              _stream(stream))
     if st != IDX_OK:
         raise IndexerError(st, "indexer_topk")
+    return idx
+
+
+def indexer_logits_topk_workspace_bytes(shape: idx_shape) -> int:
+    return load().indexer_logits_topk_workspace_bytes(ctypes.byref(shape))
+
+
+def indexer_logits_topk(q, q_sf, k, k_sf, k_scales, w, ks, ke, sm_scale, shape: idx_shape,
+                        topk: int, idx, workspace, stream=None) -> None:
+    """Top-k key columns of every row straight from the inputs, without the
+    logits (see include/dsa_indexer.h): idx is an int32 CUDA tensor
+    [B*S, >= topk] (rows contiguous at a fixed stride), workspace a uint8
+    CUDA tensor of indexer_logits_topk_workspace_bytes(shape) bytes."""
+    flat = idx.view(-1, idx.shape[-1])
+    st = load().indexer_logits_topk(_ptr(q), _ptr(q_sf), _ptr(k), _ptr(k_sf), _ptr(k_scales),
+                                    _ptr(w), _ptr(ks), _ptr(ke), ctypes.c_float(sm_scale),
+                                    ctypes.byref(shape), int(topk), _ptr(flat),
+                                    int(flat.stride(0)), _ptr(workspace),
+                                    int(workspace.numel() * workspace.element_size()),
+                                    _stream(stream))
+    if st != IDX_OK:
+        raise IndexerError(st, "indexer_logits_topk")
+
+
+def topk_case(case, t, topk: int, idx=None, workspace=None, stream=None):
+    """indexer_logits_topk on tensors made by case_to_device (contiguous keys,
+    FP32 logits shape); allocates idx and the workspace when not given."""
+    shape = make_shape(case.B, case.S, case.N, case.H, case.D, case.fmt, case.w_fmt,
+                       flags=IDX_FLAG_GROUP_ROWS if case.group_rows else 0)
+    dev = t["q"].device
+    if idx is None:
+        idx = torch.empty(case.B * case.S, topk, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(indexer_logits_topk_workspace_bytes(shape), dtype=torch.uint8,
+                                device=dev)
+    indexer_logits_topk(t["q"], t["q_sf"], t["k"], t["k_sf"], t["k_scales"], t["w"], t["ks"],
+                        t["ke"], case.sm_scale, shape, topk, idx, workspace, stream)
     return idx
 
 

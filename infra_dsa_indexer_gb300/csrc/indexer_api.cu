@@ -27,7 +27,7 @@ struct DeviceInfo {
   bool valid = false;
   int sm_count = 0;
   int cc_major = 0, cc_minor = 0;
-  bool smem_set[32] = {};  // per kernel instantiation (format, sign, output type, paging)
+  bool smem_set[128] = {};  // per kernel instantiation (format, mode, sign, output type, paging)
   bool plan_attr_set = false;
 };
 
@@ -159,12 +159,12 @@ int encode_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, in
   return r == CUDA_SUCCESS ? IDX_OK : IDX_ERR_CUDA;
 }
 
-template <int FMT, bool NEG_EPI, bool OUT_BF16, bool PAGED>
+template <int FMT, bool NEG_EPI, bool OUT_BF16, bool PAGED, int MODE = dsa::kModeLogits>
 int launch_kernel(const KernelParams& prm, int grid, DeviceInfo* di, cudaStream_t stream) {
   constexpr int smem = dsa::Layout<FMT>::kBytes;
-  auto kern = dsa::indexer_logits_kernel<FMT, NEG_EPI, OUT_BF16, PAGED>;
-  bool& attr_set =
-      di->smem_set[FMT * 8 + (NEG_EPI ? 4 : 0) + (OUT_BF16 ? 2 : 0) + (PAGED ? 1 : 0)];
+  auto kern = dsa::indexer_logits_kernel<FMT, NEG_EPI, OUT_BF16, PAGED, MODE>;
+  bool& attr_set = di->smem_set[FMT * 32 + MODE * 8 + (NEG_EPI ? 4 : 0) + (OUT_BF16 ? 2 : 0) +
+                                (PAGED ? 1 : 0)];
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
@@ -176,7 +176,11 @@ int launch_kernel(const KernelParams& prm, int grid, DeviceInfo* di, cudaStream_
 }
 
 template <int FMT, bool NEG_EPI>
-int launch(const KernelParams& prm, int grid, DeviceInfo* di, cudaStream_t stream) {
+int launch(const KernelParams& prm, int grid, DeviceInfo* di, cudaStream_t stream, int mode) {
+  if (mode == dsa::kModeSample)
+    return launch_kernel<FMT, NEG_EPI, false, false, dsa::kModeSample>(prm, grid, di, stream);
+  if (mode == dsa::kModeFilter)
+    return launch_kernel<FMT, NEG_EPI, false, false, dsa::kModeFilter>(prm, grid, di, stream);
   if (prm.block_table != nullptr)
     return prm.out_bf16 ? launch_kernel<FMT, NEG_EPI, true, true>(prm, grid, di, stream)
                         : launch_kernel<FMT, NEG_EPI, false, true>(prm, grid, di, stream);
@@ -208,7 +212,9 @@ const char* indexer_status_string(int status) {
     case IDX_ERR_CUDA: return "a CUDA runtime call failed";
     case IDX_ERR_TIMEOUT: return "a device-side wait ran out; the output of that call is invalid";
     case IDX_ERR_UNSUPPORTED: return "request not supported by this build";
-    case IDX_ERR_SCRATCH: return "call needs more scratch than the fixed no-allocation array holds";
+    case IDX_ERR_SCRATCH:
+      return "call needs more scratch than the fixed no-allocation array (or the workspace "
+             "given) holds";
     default: return "unknown status";
   }
 }
@@ -224,6 +230,18 @@ int64_t indexer_set_wait_limit_ns(int64_t ns) {
 
 namespace {
 
+// One pass of the fused top-k call (see indexer_logits_topk): which mode,
+// its per-row thresholds and candidate counts, and whether the row order of
+// a grouped call is already planned (by the pass before).
+struct PassArgs {
+  int mode = dsa::kModeLogits;
+  const float* thr = nullptr;
+  uint32_t* mask = nullptr;
+  int64_t mask_row_stride = 0;
+  int64_t out_row_stride = 0;  // overrides the shape's (elements or candidate slots)
+  bool planned = false;
+};
+
 // Validate, build the tensor maps and launch one call. `fixed_scratch` is
 // false for indexer_logits (scratch per (device, stream), allocated on first
 // use) or selects the no-allocation variant's fixed device array. `paged` is
@@ -231,7 +249,8 @@ namespace {
 int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint8_t* k_sf,
                    const float* k_scales, const void* w, const int32_t* ks, const int32_t* ke,
                    float sm_scale, int clean, void* out, const idx_shape* shape,
-                   cudaStream_t stream, bool fixed_scratch, const idx_paged* paged = nullptr) {
+                   cudaStream_t stream, bool fixed_scratch, const idx_paged* paged = nullptr,
+                   const PassArgs& pass = PassArgs()) {
   if (!shape || !q || !k || !w || !ks || !ke || !out) return IDX_ERR_NULL;
   const idx_shape sh = *shape;
   idx_paged pg{};
@@ -260,9 +279,11 @@ int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
   const int64_t q_row = sh.q_row_bytes ? sh.q_row_bytes : elem_row_bytes;
   const int64_t k_row = sh.k_row_bytes ? sh.k_row_bytes : elem_row_bytes;
   const int64_t k_batch = sh.k_batch_bytes ? sh.k_batch_bytes : k_row * sh.N;
-  const int64_t out_stride = sh.out_row_stride ? sh.out_row_stride : sh.N;
+  const int64_t out_stride =
+      pass.mode != dsa::kModeLogits ? pass.out_row_stride
+                                    : (sh.out_row_stride ? sh.out_row_stride : sh.N);
   if (q_row < elem_row_bytes || k_row < elem_row_bytes || k_batch < k_row * sh.N ||
-      out_stride < sh.N)
+      (pass.mode == dsa::kModeLogits && out_stride < sh.N))
     return IDX_ERR_SHAPE;
   const int64_t total_rows = static_cast<int64_t>(sh.B) * sh.S;
   if (total_rows * sh.H >= (int64_t(1) << 31) || static_cast<int64_t>(sh.B) * sh.N >= (int64_t(1) << 31))
@@ -338,13 +359,16 @@ int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
   prm.ke = ke;
   prm.out = out;
   prm.out_bf16 = out_bf16 ? 1 : 0;
+  prm.thr = pass.thr;
+  prm.mask = pass.mask;
+  prm.mask_row_stride = pass.mask_row_stride;
   prm.scratch = scratch;
   prm.out_row_stride = out_stride;
   prm.B = sh.B;
   prm.S = sh.S;
   prm.N = sh.N;
   prm.w_bf16 = sh.w_fmt == IDX_W_BF16;
-  prm.clean = clean != 0;
+  prm.clean = clean != 0 || pass.mode == dsa::kModeSample;
   prm.sm_scale = sm_scale;
   prm.blocks_per_batch = (sh.S + dsa::kRowsPerBlock - 1) / dsa::kRowsPerBlock;
   prm.timeout_ns = static_cast<uint64_t>(g_wait_limit_ns);
@@ -365,16 +389,19 @@ int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
   const int grid = static_cast<int>(std::min<int64_t>(di->sm_count, units));
   if (groups_rows(sh, fixed_scratch)) {
     prm.perm = scratch + kScratchInts;
-    if ((st = launch_plan(ks, ke, sh, const_cast<int32_t*>(prm.perm), di, stream))) return st;
+    if (!pass.planned &&
+        (st = launch_plan(ks, ke, sh, const_cast<int32_t*>(prm.perm), di, stream)))
+      return st;
   }
 
+  const int mode = pass.mode;
   switch (sh.fmt) {
-    case IDX_FMT_BF16: return launch<dsa::kFmtBF16, false>(prm, grid, di, stream);
-    case IDX_FMT_E4M3: return launch<dsa::kFmtE4M3, false>(prm, grid, di, stream);
-    case IDX_FMT_MXFP8: return launch<dsa::kFmtMXFP8, false>(prm, grid, di, stream);
+    case IDX_FMT_BF16: return launch<dsa::kFmtBF16, false>(prm, grid, di, stream, mode);
+    case IDX_FMT_E4M3: return launch<dsa::kFmtE4M3, false>(prm, grid, di, stream, mode);
+    case IDX_FMT_MXFP8: return launch<dsa::kFmtMXFP8, false>(prm, grid, di, stream, mode);
     case IDX_FMT_MXFP4:
-      return sm_scale < 0.f ? launch<dsa::kFmtMXFP4, true>(prm, grid, di, stream)
-                            : launch<dsa::kFmtMXFP4, false>(prm, grid, di, stream);
+      return sm_scale < 0.f ? launch<dsa::kFmtMXFP4, true>(prm, grid, di, stream, mode)
+                            : launch<dsa::kFmtMXFP4, false>(prm, grid, di, stream, mode);
     default: return IDX_ERR_UNSUPPORTED;
   }
 }
@@ -513,6 +540,120 @@ int indexer_topk(const void* logits, int logits_bf16, int64_t rows, int32_t N,
       dsa::topk_rows_kernel<kMany, false><<<grid, kMany, 0, stream>>>(logits, row_stride, N, k,
                                                                      idx, idx_stride);
   }
+  return cudaGetLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Layout of the fused top-k call's workspace, each part 256-byte aligned:
+// per-row mask words (one per 32 keys of the filtered tiles) and thresholds,
+// the compact sample rows, and a value slot for every key of the filtered
+// tiles (so no row can overflow it; only kept values are written).
+struct TopkWorkspace {
+  int64_t rows = 0, ns_cols = 0, cap = 0, mask_stride = 0;
+  int64_t off_mask = 0, off_thr = 0, off_s = 0, off_c = 0, bytes = 0;
+};
+
+int64_t align256(int64_t x) { return (x + 255) / 256 * 256; }
+
+bool topk_workspace(const idx_shape& sh, TopkWorkspace* w) {
+  if (sh.B < 1 || sh.S < 1 || sh.N < 1) return false;
+  const int64_t tiles = (static_cast<int64_t>(sh.N) + dsa::kKeysPerTile - 1) / dsa::kKeysPerTile;
+  const int64_t sample_tiles = (tiles + dsa::kSampleEvery - 1) / dsa::kSampleEvery;
+  const int64_t filtered_tiles = tiles - sample_tiles;
+  w->rows = static_cast<int64_t>(sh.B) * sh.S;
+  w->ns_cols = sample_tiles * dsa::kKeysPerTile;
+  w->cap = filtered_tiles * dsa::kKeysPerTile;
+  w->mask_stride = filtered_tiles * 4;
+  w->off_mask = 0;
+  w->off_thr = align256(w->off_mask + 4 * w->mask_stride * w->rows);
+  w->off_s = align256(w->off_thr + 4 * w->rows);
+  w->off_c = align256(w->off_s + 4 * w->rows * w->ns_cols);
+  w->bytes = align256(w->off_c + 4 * w->rows * w->cap);
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t indexer_logits_topk_workspace_bytes(const idx_shape* shape) {
+  TopkWorkspace w;
+  if (shape == nullptr || !topk_workspace(*shape, &w)) return -1;
+  return w.bytes;
+}
+
+int indexer_logits_topk(const void* q, const uint8_t* q_sf, const void* k, const uint8_t* k_sf,
+                        const float* k_scales, const void* w, const int32_t* ks,
+                        const int32_t* ke, float sm_scale, const idx_shape* shape, int32_t topk,
+                        int32_t* idx, int64_t idx_stride, void* workspace,
+                        int64_t workspace_bytes, idx_stream_t stream_) {
+  if (!shape || !idx || !workspace) return IDX_ERR_NULL;
+  if ((shape->flags & IDX_FLAG_OUT_BF16) != 0) return IDX_ERR_UNSUPPORTED;
+  if (topk < 1 || idx_stride < topk) return IDX_ERR_SHAPE;
+  TopkWorkspace ws;
+  if (!topk_workspace(*shape, &ws)) return IDX_ERR_SHAPE;
+  if (ws.rows > 0x7fffffffLL) return IDX_ERR_SHAPE;
+  if (workspace_bytes < ws.bytes) return IDX_ERR_SCRATCH;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) || (reinterpret_cast<uintptr_t>(idx) & 3u))
+    return IDX_ERR_ALIGN;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  char* base = static_cast<char*>(workspace);
+  uint32_t* mask = reinterpret_cast<uint32_t*>(base + ws.off_mask);
+  float* thr = reinterpret_cast<float*>(base + ws.off_thr);
+  float* smp = reinterpret_cast<float*>(base + ws.off_s);
+  float* kept = reinterpret_cast<float*>(base + ws.off_c);
+  int sms = 0;
+  {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return IDX_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo* di = nullptr;
+    int st = get_device_info(dev, &di);
+    if (st) return st;
+    sms = di->sm_count;
+  }
+  // 1. the sample pass: every kSampleEvery-th key tile, compact FP32 rows
+  PassArgs pass;
+  pass.mode = dsa::kModeSample;
+  pass.out_row_stride = ws.ns_cols;
+  int st = enqueue_logits(q, q_sf, k, k_sf, k_scales, w, ks, ke, sm_scale, 1, smp, shape, stream,
+                          false, nullptr, pass);
+  if (st) return st;
+  if (cudaMemsetAsync(mask, 0, 4 * ws.mask_stride * ws.rows, stream) != cudaSuccess)
+    return IDX_ERR_CUDA;
+  // 2. each row's threshold: the topk-th largest of its sample
+  const dim3 grid(static_cast<unsigned>(ws.rows));
+  const bool few = ws.rows <= 2LL * sms;
+  constexpr int kMany = dsa::kTopkThreads, kFew = dsa::kTopkThreadsFew;
+  if (few)
+    dsa::topk_threshold_kernel<kFew><<<grid, kFew, 0, stream>>>(smp, ws.ns_cols,
+                                                              static_cast<int>(ws.ns_cols), topk, thr);
+  else
+    dsa::topk_threshold_kernel<kMany><<<grid, kMany, 0, stream>>>(smp, ws.ns_cols,
+                                                                static_cast<int>(ws.ns_cols), topk, thr);
+  if (cudaGetLastError() != cudaSuccess) return IDX_ERR_CUDA;
+  // 3. the other key tiles: append the values at or above the threshold
+  pass.mode = dsa::kModeFilter;
+  pass.out_row_stride = ws.cap;
+  pass.thr = thr;
+  pass.mask = mask;
+  pass.mask_row_stride = ws.mask_stride;
+  pass.planned = true;  // a grouped call's row order is the sample pass's
+  if ((st = enqueue_logits(q, q_sf, k, k_sf, k_scales, w, ks, ke, sm_scale, 1, kept, shape, stream,
+                           false, nullptr, pass)))
+    return st;
+  // 4. the top-k of sample and candidates
+  if (few)
+    dsa::topk_merge_kernel<kFew><<<grid, kFew, 0, stream>>>(
+        smp, ws.ns_cols, static_cast<int>(ws.ns_cols), kept, ws.cap, mask, ws.mask_stride,
+        dsa::kSampleEvery, topk, idx, idx_stride);
+  else
+    dsa::topk_merge_kernel<kMany><<<grid, kMany, 0, stream>>>(
+        smp, ws.ns_cols, static_cast<int>(ws.ns_cols), kept, ws.cap, mask, ws.mask_stride,
+        dsa::kSampleEvery, topk, idx, idx_stride);
   return cudaGetLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }
 

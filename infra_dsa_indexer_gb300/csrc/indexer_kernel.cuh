@@ -79,6 +79,39 @@ constexpr int kSfbBytes = kBlockN * 4;           // one word per (row, head)
 enum : int { kFmtBF16 = 0, kFmtE4M3 = 1, kFmtMXFP8 = 2, kFmtMXFP4 = 3 };
 enum : int { kErrTimeout = 8, kErrAlign = 4 };
 
+// What a launch computes (the fused top-k call runs the last two):
+//  kModeLogits  every key tile; the logits go to `out` (the indexer call)
+//  kModeSample  key tiles t with t % kSampleEvery == 0; their logits go to a
+//               compact row of ceil(tiles / kSampleEvery) * 128 columns
+//               (column (t / kSampleEvery) * 128 + j % 128), -inf outside
+//               the window and past N
+//  kModeFilter  the other key tiles; only in-window logits >= the row's
+//               threshold thr[row] are kept. Key j of filtered tile t keeps
+//               its value at slot rank(t) * 128 + j % 128 of the row's kept
+//               values (rank(t): position of t among the filtered tiles),
+//               and 32-key group g = rank(t) * 4 + (j % 128) / 32 has a mask
+//               word (bit j % 32 set: kept) in the row's masks
+enum : int { kModeLogits = 0, kModeSample = 1, kModeFilter = 2 };
+constexpr int kSampleEvery = 4;
+
+template <int MODE>
+__device__ __forceinline__ bool tile_in_mode(int t) {
+  if constexpr (MODE == kModeSample) return t % kSampleEvery == 0;
+  else if constexpr (MODE == kModeFilter) return t % kSampleEvery != 0;
+  else return true;
+}
+// First tile >= t that the mode computes.
+template <int MODE>
+__device__ __forceinline__ int first_tile(int t) {
+  if constexpr (MODE == kModeSample) return (t + kSampleEvery - 1) / kSampleEvery * kSampleEvery;
+  else if constexpr (MODE == kModeFilter) return t % kSampleEvery == 0 ? t + 1 : t;
+  else return t;
+}
+template <int MODE>
+__device__ __forceinline__ int next_tile(int t) {
+  return first_tile<MODE>(t + 1);
+}
+
 struct UnitInfo {
   int32_t stop;
   int32_t b;
@@ -115,9 +148,13 @@ struct KernelParams {
   int32_t page_size;     // multiple of 64
   int32_t table_stride;
   int32_t num_pages;     // page numbers are clamped to [0, num_pages)
-  void* out;         // FP32, or BF16 when out_bf16
+  void* out;         // FP32, or BF16 when out_bf16; the compact sample rows
+                     // (kModeSample) or the (value, column) candidates (kModeFilter)
   int32_t* scratch;  // [0] unit counter, [1] finished CTAs, [2] error word
-  int64_t out_row_stride;
+  int64_t out_row_stride;  // elements (kModeFilter: candidate slots per row)
+  const float* thr;        // kModeFilter: per-row threshold
+  uint32_t* mask;          // kModeFilter: per-row group masks (zeroed before)
+  int64_t mask_row_stride; // kModeFilter: mask words per row
   int32_t B, S, N;
   int32_t w_bf16;
   int32_t out_bf16;  // selects the OUT_BF16 instantiation
@@ -331,9 +368,11 @@ __device__ __forceinline__ void mma_step(uint32_t d_tmem, uint64_t a_desc, uint6
 // kind has no negate bit); every other case negates the MMA's A operand.
 // OUT_BF16: the logits are stored as BF16 (round to nearest even).
 // PAGED: the keys (and key scales) are read through the page table.
-template <int FMT, bool NEG_EPI, bool OUT_BF16, bool PAGED>
+// MODE: kModeLogits, or one of the two passes of the fused top-k call.
+template <int FMT, bool NEG_EPI, bool OUT_BF16, bool PAGED, int MODE = kModeLogits>
 __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
     indexer_logits_kernel(const __grid_constant__ KernelParams p) {
+  static_assert(MODE == kModeLogits || (!OUT_BF16 && !PAGED), "fused top-k: FP32, contiguous keys");
   using T = Traits<FMT>;
   using L = Layout<FMT>;
   constexpr int kNumEpiWarps = L::kNumEpiWarps;
@@ -629,7 +668,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       const QInfo& qi = qinfo[slot];
       if (qi.stop) break;
       const int c0 = qi.c0, c1 = qi.c1, b = qi.b;
-      for (int t = c0; t < c1; ++t, ++kiter) {
+      for (int t = first_tile<MODE>(c0); t < c1; t = next_tile<MODE>(t), ++kiter) {
         const int st = kiter % T::kStages;
         if (lane == 0)
           ok = mbar_wait(&k_empty[st], ((kiter / T::kStages) & 1) ^ 1, abort_flag, p.timeout_ns);
@@ -716,9 +755,10 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       const QInfo& qi = qinfo[slot];
       if (qi.stop) break;
       const int c0 = qi.c0, c1 = qi.c1;
+      const int tf = first_tile<MODE>(c0);  // the unit's first tile in this mode
       const uint64_t b_base = q_desc0 + ((slot * L::kQBlockBytes) >> 4);
       bool ok = true;
-      for (int t = c0; t < c1; ++t, ++kiter, ++aiter) {
+      for (int t = tf; t < c1; t = next_tile<MODE>(t), ++kiter, ++aiter) {
         const int st = kiter % T::kStages;
         const int acc = aiter % kAccBufs;
         const uint32_t kpar = (kiter / T::kStages) & 1;
@@ -743,7 +783,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
           fence_proxy_async_smem();
           sfa = tmem_base + kSfaCol + 4 * (kiter & 1);
           sfb = tmem_base + kSfbCol + 8 * (units_mma & 1);
-          if (t == c0) {
+          if (t == tf) {
             const uint64_t d = sfb_desc0 + ((slot * kSfbBytes) >> 4);
             tc_cp_32x128b_warpx4(sfb, d);
             tc_cp_32x128b_warpx4(sfb + 4, d + (512 >> 4));
@@ -777,7 +817,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         tc_commit(&k_empty[st]);
         tc_commit(&acc_full[acc]);
       }
-      if (c1 > c0) ++units_mma;
+      if (tf < c1) ++units_mma;
       if (!ok) {
         raise_error(p.scratch, abort_flag, kErrTimeout);
         break;
@@ -819,6 +859,10 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       char* orow[R];
       bool any_row = false;
       constexpr bool obf = OUT_BF16;
+      // bytes per output slot: logits, compact sample logits, or candidates
+      constexpr int kSlot = obf ? 2 : 4;
+      float thr[R];      // kModeFilter: the rows' thresholds
+      int32_t rowid[R];  // kModeFilter: the rows (-1: absent)
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         lo[r] = in.lo[r0 + r];
@@ -826,15 +870,20 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         const int row = in.row[r0 + r];
         orow[r] = row < 0 ? (r > 0 ? orow[0] : nullptr)
                           : static_cast<char*>(p.out) +
-                                static_cast<int64_t>(row) * p.out_row_stride * (obf ? 2 : 4);
+                                static_cast<int64_t>(row) * p.out_row_stride * kSlot;
         any_row |= row >= 0;
+        rowid[r] = row;
+        if constexpr (MODE == kModeFilter) thr[r] = row >= 0 ? __ldg(p.thr + row) : 0.f;
       }
       const int store_lim = any_row ? p.N : 0;
       const float* wrows = reinterpret_cast<const float*>(wbuf + slot * L::kWBytes) + r0 * kHeads;
-      if (p.clean && (flags & 1)) {
+      // Compact sample column of the first key of tile t (kModeSample).
+      auto sample_col = [](int t) { return first_tile<kModeSample>(t) / kSampleEvery * kKeysPerTile; };
+      if (p.clean && (flags & 1) && MODE != kModeFilter) {
+        const int end = MODE == kModeSample ? sample_col(t0) : t0 * kKeysPerTile;
 #pragma unroll
         for (int r = 0; r < R; ++r)
-          if (orow[r] != nullptr) fill_neg_inf(orow[r], 0, t0 * kKeysPerTile, tid128, obf);
+          if (orow[r] != nullptr) fill_neg_inf(orow[r], 0, end, tid128, obf);
       }
       // Per-key scale (E4M3), loaded one tile ahead so that its latency
       // overlaps the previous tile instead of stalling the loop head. Paged
@@ -861,7 +910,8 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         return __ldg(p.k_scales + static_cast<int64_t>(page) * p.page_size + jj % p.page_size);
       };
       int page_ahead = PAGED ? load_page(c0 + 1) : -1;
-      float kscale_next = PAGED ? scale_in_page(c0, load_page(c0)) : load_kscale(c0);
+      float kscale_next =
+          PAGED ? scale_in_page(c0, load_page(c0)) : load_kscale(first_tile<MODE>(c0));
       bool ok = true;
       if (PAGED && !any_row) {
         // Every row of this warp is past S (a partial last block; decode with
@@ -879,7 +929,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
           if (lane == 0) mbar_arrive(&acc_empty[aiter % kAccBufs]);
         }
       } else {
-        for (int t = c0; t < c1; ++t, ++aiter) {
+        for (int t = first_tile<MODE>(c0); t < c1; t = next_tile<MODE>(t), ++aiter) {
           const int acc = aiter % kAccBufs;
           const int j = t * kKeysPerTile + quarter * 32 + lane;
           const float kscale = kscale_next;
@@ -887,7 +937,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
             kscale_next = scale_in_page(t + 1, page_ahead);
             page_ahead = load_page(t + 2);
           } else {
-            kscale_next = load_kscale(t + 1);
+            kscale_next = load_kscale(next_tile<MODE>(t));
           }
           if (!mbar_wait(&acc_full[acc], (aiter / kAccBufs) & 1, abort_flag, p.timeout_ns)) {
             ok = false;
@@ -911,14 +961,41 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
           float sums[R];
 #pragma unroll
           for (int r = 0; r < R; ++r) sums[r] = racc[r].total();
-          if (j < store_lim) {
+          if constexpr (MODE == kModeLogits) {
+            if (j < store_lim) {
 #pragma unroll
-            for (int r = R - 1; r >= 0; --r) {
-              const float v = (j >= lo[r] && j < hi[r]) ? sums[r] * (sm_abs * kscale) : ninf;
-              if (obf)
-                st_cs_b16(orow[r] + 2 * static_cast<int64_t>(j), f32_to_bf16_rn(v));
-              else
-                __stcs(reinterpret_cast<float*>(orow[r]) + j, v);
+              for (int r = R - 1; r >= 0; --r) {
+                const float v = (j >= lo[r] && j < hi[r]) ? sums[r] * (sm_abs * kscale) : ninf;
+                if (obf)
+                  st_cs_b16(orow[r] + 2 * static_cast<int64_t>(j), f32_to_bf16_rn(v));
+                else
+                  __stcs(reinterpret_cast<float*>(orow[r]) + j, v);
+              }
+            }
+          } else if constexpr (MODE == kModeSample) {
+            // every compact column of a sample tile is written: -inf past N
+            if (any_row) {
+              const int col = t / kSampleEvery * kKeysPerTile + quarter * 32 + lane;
+#pragma unroll
+              for (int r = R - 1; r >= 0; --r) {
+                const float v = (j < p.N && j >= lo[r] && j < hi[r]) ? sums[r] * (sm_abs * kscale)
+                                                                     : ninf;
+                __stcs(reinterpret_cast<float*>(orow[r]) + col, v);
+              }
+            }
+          } else {
+            // Keep the in-window values >= the row's threshold at their own
+            // slots, and the group's mask word (no atomics: slots and word
+            // belong to this (row, tile, quarter) alone).
+            const int grp = (t - t / kSampleEvery - 1) * 4 + quarter;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              const float v = sums[r] * (sm_abs * kscale);
+              const bool pass = rowid[r] >= 0 && j < p.N && j >= lo[r] && j < hi[r] && v >= thr[r];
+              const uint32_t m = __ballot_sync(0xffffffffu, pass);
+              if (pass) reinterpret_cast<float*>(orow[r])[grp * 32 + lane] = v;
+              if (lane == 0 && m != 0u)
+                p.mask[static_cast<int64_t>(rowid[r]) * p.mask_row_stride + grp] = m;
             }
           }
         }
@@ -927,10 +1004,12 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         raise_error(p.scratch, abort_flag, kErrTimeout);
         break;
       }
-      if (p.clean && (flags & 2)) {
+      if (p.clean && (flags & 2) && MODE != kModeFilter) {
+        const int from = MODE == kModeSample ? sample_col(t1) : t1 * kKeysPerTile;
+        const int to = MODE == kModeSample ? static_cast<int>(p.out_row_stride) : p.N;
 #pragma unroll
         for (int r = 0; r < R; ++r)
-          if (orow[r] != nullptr) fill_neg_inf(orow[r], t1 * kKeysPerTile, p.N, tid128, obf);
+          if (orow[r] != nullptr) fill_neg_inf(orow[r], from, to, tid128, obf);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&unit_empty[slot]);

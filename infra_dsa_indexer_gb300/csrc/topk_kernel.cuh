@@ -208,16 +208,105 @@ __device__ __forceinline__ void topk_select_in_smem(TopkShared& sh, const uint32
   __syncthreads();
 }
 
-// Fast path (sample select). Runs of 8 consecutive columns spread over the
+// Rows the selection reads, each a sequence of n (column, key) elements
+// with random access by position e (key(e), col(e)) and a block-wide sweep
+// (for_each(f): f(column, key) for every element).
+
+// A dense logits row: element e is column e.
+template <bool BF16_IN>
+struct DenseRow {
+  const char* rp;
+  int n;
+  __device__ __forceinline__ uint32_t key(int e) const { return load_key<BF16_IN>(rp, e); }
+  __device__ __forceinline__ int col(int e) const { return e; }
+  template <int NT, typename F>
+  __device__ __forceinline__ void for_each(F&& f) const {
+    for_each_key<NT, BF16_IN>(rp, n, f);
+  }
+};
+
+// The fused top-k call's row: a compact FP32 sample row (element e < ns is
+// column (e / 128) * 128 * sample_every + e % 128) followed by the kept-value
+// slots of the filtered tiles, 32-slot group g with mask word mask[g]: slot
+// 32 g + l holds a kept value iff bit l is set, for column
+// tile(g / 4) * 128 + (g % 4) * 32 + l, where tile(r) is the r-th tile not
+// sampled; unset slots are not elements (key 0).
+struct MergeRow {
+  const float* s;
+  int ns;
+  const float* kept;
+  const uint32_t* mask;
+  int ngroups;
+  int sample_every;
+  int n;
+  __device__ __forceinline__ int sample_col(int e) const {
+    return (e >> 7) * (128 * sample_every) + (e & 127);
+  }
+  __device__ __forceinline__ int kept_col(int g, int l) const {
+    const int r = g >> 2;  // rank among the filtered tiles
+    const int per = sample_every - 1;
+    const int tile = (r / per) * sample_every + r % per + 1;
+    return tile * 128 + (g & 3) * 32 + l;
+  }
+  __device__ __forceinline__ uint32_t key(int e) const {
+    if (e < ns) return order_key(__float_as_uint(__ldg(s + e)));
+    const int i = e - ns;
+    return (__ldg(mask + (i >> 5)) >> (i & 31)) & 1u
+               ? order_key(__float_as_uint(__ldg(kept + i)))
+               : 0u;
+  }
+  __device__ __forceinline__ int col(int e) const {
+    return e < ns ? sample_col(e) : kept_col((e - ns) >> 5, (e - ns) & 31);
+  }
+  template <int NT, typename F>
+  __device__ __forceinline__ void for_each(F&& f) const {
+    for_each_key<NT, false>(reinterpret_cast<const char*>(s), ns,
+                            [&](int e, uint32_t key) { f(sample_col(e), key); });
+    // A warp takes 32 groups at a time: lane l reads mask word g0 + l, then
+    // every lane loads its slot of each of the 32 groups where that slot is
+    // set (32 independent loads in flight), then visits them.
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int g0 = warp * 32; g0 < ngroups; g0 += NT) {
+      const uint32_t mw = g0 + lane < ngroups ? __ldg(mask + g0 + lane) : 0u;
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const uint32_t m = __shfl_sync(0xffffffffu, mw, i);
+        v[i] = (m >> lane) & 1u ? __ldg(kept + (g0 + i) * 32 + lane) : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const uint32_t m = __shfl_sync(0xffffffffu, mw, i);
+        if ((m >> lane) & 1u) f(kept_col(g0 + i, lane), order_key(__float_as_uint(v[i])));
+      }
+    }
+  }
+};
+
+// The value of an order-preserving key.
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+// Where a selection puts its answer: the k column indices of the row
+// (kth == nullptr), or only the k-th largest value (a lower bound of it, or
+// -inf when the row has no more than k finite values) in *kth.
+struct TopkOut {
+  int32_t* idx;
+  float* kth;
+};
+
+// Fast path (sample select). Runs of 8 consecutive elements spread over the
 // row (in shared memory) give a threshold a little
-// below the expected k-th largest value; one sweep compacts every column at
+// below the expected k-th largest value; one sweep compacts every element at
 // or above it, and the exact selection runs on those in shared memory.
 // Returns false, with nothing written, when the sample misjudged: fewer than
-// k columns reach the threshold although it excluded finite values, or more
-// columns than fit.
-template <int NT, bool BF16_IN>
-__device__ bool topk_sample_select(TopkShared& sh, const char* rp, int N, int k, int32_t* out) {
+// k elements reach the threshold although it excluded finite values, or more
+// elements than fit.
+template <int NT, typename Src>
+__device__ bool topk_sample_select(TopkShared& sh, const Src& src, int k, TopkOut o) {
   const int tid = threadIdx.x;
+  const int N = src.n;
   constexpr int kRun = 8;
   // Sample size: enough runs that the k-th column's expected sample rank,
   // m = k * ns / N, is about 128 (spread ~9%), at least 512 keys and at
@@ -237,7 +326,7 @@ __device__ bool topk_sample_select(TopkShared& sh, const char* rp, int N, int k,
   uint32_t nfin_local = 0;
   for (int s = tid; s < runs * kRun; s += NT) {
     const int j = (s / kRun) * step + s % kRun;
-    const uint32_t key = j < N ? load_key<BF16_IN>(rp, j) : 0u;
+    const uint32_t key = j < N ? src.key(j) : 0u;
     const bool fin = key > kNegInfKey;
     sh.cand_key[s] = fin ? key : 0u;  // 0 ranks below every finite key
     nfin_local += fin ? 1u : 0u;
@@ -272,7 +361,7 @@ __device__ bool topk_sample_select(TopkShared& sh, const char* rp, int N, int k,
     sh.ties = 0;
   }
   __syncthreads();
-  for_each_key<NT, BF16_IN>(rp, N, [&](int j, uint32_t key) {
+  src.template for_each<NT>([&](int j, uint32_t key) {
     if (key < t_est) return;
     const uint32_t pos = atomicAdd(&sh.ncand, 1u);
     if (pos < static_cast<uint32_t>(kTopkCand)) {
@@ -286,36 +375,35 @@ __device__ bool topk_sample_select(TopkShared& sh, const char* rp, int N, int k,
   if (nc < static_cast<uint32_t>(k)) {
     // right only when the threshold let every finite value through
     if (t_est != kNegInfKey + 1u) return false;
-    for (uint32_t c = tid; c < nc; c += NT) out[c] = sh.cand_idx[c];
-    for (int i = static_cast<int>(nc) + tid; i < k; i += NT) out[i] = -1;
+    if (o.kth != nullptr) {
+      if (tid == 0) *o.kth = __int_as_float(0xff800000);
+      return true;
+    }
+    for (uint32_t c = tid; c < nc; c += NT) o.idx[c] = sh.cand_idx[c];
+    for (int i = static_cast<int>(nc) + tid; i < k; i += NT) o.idx[i] = -1;
     return true;
   }
   topk_select_in_smem<NT>(sh, sh.cand_key, nc);
   const uint32_t thr = sh.prefix, ties = sh.need;
+  if (o.kth != nullptr) {
+    if (tid == 0) *o.kth = key_value(thr);
+    return true;
+  }
   for (uint32_t c = tid; c < nc; c += NT) {
     const uint32_t key = sh.cand_key[c];
     bool t = key > thr;
     if (key == thr) t = atomicAdd(&sh.ties, 1u) < ties;
-    if (t) out[atomicAdd(&sh.out, 1u)] = sh.cand_idx[c];
+    if (t) o.idx[atomicAdd(&sh.out, 1u)] = sh.cand_idx[c];
   }
   return true;
 }
 
-// NT threads per CTA and 2048 / NT CTAs per SM (the register cap this
-// implies costs a few spills). With many rows, 512 threads and four CTAs
-// per SM: the shared-memory phases of one row overlap the sweeps of the
-// others. With too few rows to fill the GPU (decode), 1024 threads per row
-// shorten each row's sweeps and shared-memory passes instead.
-template <int NT, bool BF16_IN>
-__global__ void __launch_bounds__(NT, 2048 / NT)
-    topk_rows_kernel(const void* __restrict__ logits, int64_t row_stride, int N, int k,
-                     int32_t* __restrict__ idx, int64_t idx_stride) {
-  __shared__ TopkShared sh;
+// The whole selection of one row by the CTA: the sample-select fast path,
+// else an exact radix select by sweeps over the row.
+template <int NT, typename Src>
+__device__ void topk_row(TopkShared& sh, const Src& src, int k, TopkOut o) {
   const int tid = threadIdx.x;
-  const int64_t row = blockIdx.x;
-  const char* rp = reinterpret_cast<const char*>(logits) + row * row_stride * (BF16_IN ? 2 : 4);
-  int32_t* out = idx + row * idx_stride;
-  if (topk_sample_select<NT, BF16_IN>(sh, rp, N, k, out)) return;
+  if (topk_sample_select<NT>(sh, src, k, o)) return;
 
   // Exact path: radix select by sweeps over the row.
   __syncthreads();
@@ -334,7 +422,7 @@ __global__ void __launch_bounds__(NT, 2048 / NT)
     const int shift = 24 - 8 * pass;
     topk_clear_hist<NT>(sh);
     const uint32_t prefix = sh.prefix, mask = sh.mask;
-    for_each_key<NT, BF16_IN>(rp, N, [&](int, uint32_t key) {
+    src.template for_each<NT>([&](int, uint32_t key) {
       if (key > kNegInfKey && (key & mask) == prefix)
         atomicAdd(&sh.hist[(key >> shift) & 255u], 1u);
     });
@@ -343,18 +431,24 @@ __global__ void __launch_bounds__(NT, 2048 / NT)
   }
 
   if (sh.finite <= static_cast<uint32_t>(k)) {
+    if (o.kth != nullptr) {
+      // no more than k finite values: no threshold excludes any of them
+      if (tid == 0) *o.kth = __int_as_float(0xff800000);
+      return;
+    }
     // every finite value is selected
-    for_each_key<NT, BF16_IN>(rp, N, [&](int j, uint32_t key) {
-      if (key > kNegInfKey) out[atomicAdd(&sh.out, 1u)] = j;
+    src.template for_each<NT>([&](int j, uint32_t key) {
+      if (key > kNegInfKey) o.idx[atomicAdd(&sh.out, 1u)] = j;
     });
   } else {
     // Sweep 3: columns above the boundary bin are in; the bin is compacted.
     const uint32_t hi16 = sh.prefix >> 16;
-    for_each_key<NT, BF16_IN>(rp, N, [&](int j, uint32_t key) {
+    const bool want_idx = o.kth == nullptr;
+    src.template for_each<NT>([&](int j, uint32_t key) {
       if (key <= kNegInfKey) return;
       const uint32_t top = key >> 16;
       if (top > hi16) {
-        out[atomicAdd(&sh.out, 1u)] = j;
+        if (want_idx) o.idx[atomicAdd(&sh.out, 1u)] = j;
       } else if (top == hi16) {
         const uint32_t pos = atomicAdd(&sh.ncand, 1u);
         if (pos < static_cast<uint32_t>(kTopkCand)) {
@@ -377,7 +471,7 @@ __global__ void __launch_bounds__(NT, 2048 / NT)
           if ((key & mask) == prefix) atomicAdd(&sh.hist[(key >> shift) & 255u], 1u);
         }
       } else {
-        for_each_key<NT, BF16_IN>(rp, N, [&](int, uint32_t key) {
+        src.template for_each<NT>([&](int, uint32_t key) {
           if (key > kNegInfKey && (key & mask) == prefix)
             atomicAdd(&sh.hist[(key >> shift) & 255u], 1u);
         });
@@ -386,22 +480,72 @@ __global__ void __launch_bounds__(NT, 2048 / NT)
     }
     // The boundary bin's share: keys above the threshold, then enough ties.
     const uint32_t thr = sh.prefix, ties = sh.need;
+    if (!want_idx) {
+      if (tid == 0) *o.kth = key_value(thr);
+      return;
+    }
     auto take = [&](int j, uint32_t key) {
       if ((key >> 16) != hi16) return;
       bool t = key > thr;
       if (key == thr) t = atomicAdd(&sh.ties, 1u) < ties;
-      if (t) out[atomicAdd(&sh.out, 1u)] = j;
+      if (t) o.idx[atomicAdd(&sh.out, 1u)] = j;
     };
     if (in_smem) {
       for (uint32_t c = tid; c < nc; c += NT) take(sh.cand_idx[c], sh.cand_key[c]);
     } else {
-      for_each_key<NT, BF16_IN>(rp, N, [&](int j, uint32_t key) {
+      src.template for_each<NT>([&](int j, uint32_t key) {
         if (key > kNegInfKey) take(j, key);
       });
     }
   }
   __syncthreads();
-  for (int i = static_cast<int>(sh.out) + tid; i < k; i += NT) out[i] = -1;
+  for (int i = static_cast<int>(sh.out) + tid; i < k; i += NT) o.idx[i] = -1;
+}
+
+// NT threads per CTA and 2048 / NT CTAs per SM (the register cap this
+// implies costs a few spills). With many rows, 512 threads and four CTAs
+// per SM: the shared-memory phases of one row overlap the sweeps of the
+// others. With too few rows to fill the GPU (decode), 1024 threads per row
+// shorten each row's sweeps and shared-memory passes instead.
+template <int NT, bool BF16_IN>
+__global__ void __launch_bounds__(NT, 2048 / NT)
+    topk_rows_kernel(const void* __restrict__ logits, int64_t row_stride, int N, int k,
+                     int32_t* __restrict__ idx, int64_t idx_stride) {
+  __shared__ TopkShared sh;
+  const int64_t row = blockIdx.x;
+  const DenseRow<BF16_IN> src{
+      reinterpret_cast<const char*>(logits) + row * row_stride * (BF16_IN ? 2 : 4), N};
+  topk_row<NT>(sh, src, k, TopkOut{idx + row * idx_stride, nullptr});
+}
+
+// Fused top-k, pass 2: the k-th largest value of each compact sample row
+// (-inf if it holds no more than k finite values). k sample values of the
+// row are logits of the row, so its k-th largest logit is at least this.
+template <int NT>
+__global__ void __launch_bounds__(NT, 2048 / NT)
+    topk_threshold_kernel(const float* __restrict__ s, int64_t s_stride, int ns, int k,
+                          float* __restrict__ thr) {
+  __shared__ TopkShared sh;
+  const int64_t row = blockIdx.x;
+  const DenseRow<false> src{reinterpret_cast<const char*>(s + row * s_stride), ns};
+  topk_row<NT>(sh, src, k, TopkOut{nullptr, thr + row});
+}
+
+// Fused top-k, pass 4: the k largest of a row's sample values and its kept
+// candidates (every logit of the row at or above the threshold is in one
+// of the two), as column indices.
+template <int NT>
+__global__ void __launch_bounds__(NT, 2048 / NT)
+    topk_merge_kernel(const float* __restrict__ s, int64_t s_stride, int ns,
+                      const float* __restrict__ kept, int64_t kept_stride,
+                      const uint32_t* __restrict__ mask, int64_t mask_stride, int sample_every,
+                      int k, int32_t* __restrict__ idx, int64_t idx_stride) {
+  __shared__ TopkShared sh;
+  const int64_t row = blockIdx.x;
+  const int ngroups = static_cast<int>(mask_stride);
+  const MergeRow src{s + row * s_stride, ns, kept + row * kept_stride, mask + row * mask_stride,
+                     ngroups, sample_every, ns + 32 * ngroups};
+  topk_row<NT>(sh, src, k, TopkOut{idx + row * idx_stride, nullptr});
 }
 
 }  // namespace dsa

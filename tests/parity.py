@@ -68,3 +68,28 @@ def compare(gpu_rows, ref, den, *, check_outside=True, tol=REL_TOL, out_rounding
         print(f"parity {label}: max err / den {worst:.3e}, / den_abs {worst_abs:.3e}")
     assert worst <= tol, f"max relative error {worst:.3e} > {tol}"
     return worst
+
+
+def check_topk(vals, sel, k):
+    """A top-k selection against the values it was taken from.
+
+    vals [R, N] float64 (-inf allowed), sel [R, >= k] int32 column indices.
+    Several selections are correct when values tie at the threshold, so what
+    is checked is what is unique: with T the k-th largest finite value of a
+    row, k distinct valid columns (or every finite column and -1 padding when
+    there are fewer than k), every value above T, and only values >= T."""
+    for r in range(vals.shape[0]):
+        v = vals[r]
+        finite = np.flatnonzero(np.isfinite(v))
+        s = sel[r][:k]
+        picked = s[s >= 0]
+        assert np.all(s[len(picked):] == -1), f"row {r}: -1 not at the end"
+        assert len(np.unique(picked)) == len(picked), f"row {r}: repeated index"
+        if len(finite) <= k:
+            assert set(picked.tolist()) == set(finite.tolist()), f"row {r}"
+            continue
+        assert len(picked) == k, f"row {r}: {len(picked)} of {k}"
+        thr = np.sort(v[finite])[::-1][k - 1]
+        assert np.all(v[picked] >= thr), f"row {r}: below the threshold"
+        above = np.flatnonzero(v > thr)
+        assert set(above.tolist()) <= set(picked.tolist()), f"row {r}: misses a larger value"

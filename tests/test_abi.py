@@ -167,3 +167,45 @@ def test_topk_host_validation(lib, args, status):
     a.update(args)
     assert lib.indexer_topk(a["logits"], a["bf16"], a["rows"], a["N"], a["row_stride"], a["k"],
                             a["idx"], a["idx_stride"], None) == status
+
+
+def test_fused_topk_workspace_bytes(lib):
+    """The fused call's workspace holds per row a mask word per 32 keys of the
+    filtered tiles, the threshold, the sampled tiles (one 128-key tile in four,
+    4 bytes a key) and a value slot for every key of the other tiles, each part
+    256-byte aligned."""
+    def expect(B, S, N):
+        tiles = -(-N // 128)
+        st = -(-tiles // 4)
+        ft = tiles - st
+        rows = B * S
+        a = lambda x: -(-x // 256) * 256
+        off_thr = a(4 * ft * 4 * rows)
+        off_s = a(off_thr + 4 * rows)
+        off_c = a(off_s + 4 * rows * st * 128)
+        return a(off_c + 4 * rows * ft * 128)
+    for B, S, N in [(1, 1, 1), (1, 4, 127), (2, 40, 3000), (1, 8192, 65536), (3, 5, 513)]:
+        assert binding.indexer_logits_topk_workspace_bytes(shp(B=B, S=S, N=N)) == expect(B, S, N)
+    assert lib.indexer_logits_topk_workspace_bytes(None) == -1
+    assert binding.indexer_logits_topk_workspace_bytes(shp(N=0)) == -1
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(idx=None), 1),
+    (dict(workspace=None), 1),
+    (dict(shape=None), 1),
+    (dict(topk=0), 2),
+    (dict(idx_stride=7), 2),                                 # < topk
+    (dict(flags=2), 9),                                      # BF16 logits: no logits here
+    (dict(workspace_bytes=1024), 10),                        # too small
+    (dict(workspace=ctypes.c_void_p(0x1010)), 4),            # not 256-byte aligned
+])
+def test_fused_topk_host_validation(lib, over, status):
+    shape = shp(flags=over.pop("flags", 0))
+    a = dict(topk=8, idx=FAKE, idx_stride=8, workspace=ctypes.c_void_p(0x100000),
+             workspace_bytes=1 << 40, shape=ctypes.byref(shape))
+    a.update(over)
+    assert lib.indexer_logits_topk(FAKE, None, FAKE, None, None, FAKE, FAKE, FAKE,
+                                   ctypes.c_float(0.1), a["shape"], a["topk"], a["idx"],
+                                   a["idx_stride"], a["workspace"], a["workspace_bytes"],
+                                   None) == status

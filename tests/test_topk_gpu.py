@@ -13,28 +13,9 @@ import pytest
 import torch
 
 from infra_dsa_indexer_gb300 import binding, synth
-from parity import REL_TOL, oracle_rows
+from parity import REL_TOL, check_topk, oracle_rows
 
 pytestmark = pytest.mark.gpu
-
-
-def check_topk(vals, sel, k):
-    """vals [R, N] float64 (-inf allowed), sel [R, k] int32."""
-    for r in range(vals.shape[0]):
-        v = vals[r]
-        finite = np.flatnonzero(np.isfinite(v))
-        s = sel[r]
-        picked = s[s >= 0]
-        assert np.all(s[len(picked):] == -1), f"row {r}: -1 not at the end"
-        assert len(np.unique(picked)) == len(picked), f"row {r}: repeated index"
-        if len(finite) <= k:
-            assert set(picked.tolist()) == set(finite.tolist()), f"row {r}"
-            continue
-        assert len(picked) == k, f"row {r}: {len(picked)} of {k}"
-        thr = np.sort(v[finite])[::-1][k - 1]
-        assert np.all(v[picked] >= thr), f"row {r}: below the threshold"
-        above = np.flatnonzero(v > thr)
-        assert set(above.tolist()) <= set(picked.tolist()), f"row {r}: misses a larger value"
 
 
 @pytest.mark.parametrize("N,k", [(1, 1), (100, 7), (100, 150), (5000, 2048), (65536, 2048),
