@@ -63,7 +63,17 @@ L2_FLUSH_BYTES = 256 << 20
 KERNEL_FILES = ("indexer_kernel.cuh", "ptx.cuh", "plan_kernel.cuh")
 # DRAM bytes (read + write) of one logits-kernel launch from an ncu capture,
 # keyed by workload, with the kernel-source digest it was taken on.
-PROFILED_TRAFFIC = {}
+PROFILED_TRAFFIC = {
+    "bf16_batched_causal_4096": ("778e9c37d10780c0", 137480960 + 79307008),
+    "fp8_per_token_2048x32768": ("778e9c37d10780c0", 21691648 + 207704576),
+    "mxfp8_2048x32768": ("778e9c37d10780c0", 22223360 + 207711232),
+    "mxfp4_2048x32768": ("778e9c37d10780c0", 11789056 + 207355648),
+    "paged_fp8_decode_64x2_32768": ("778e9c37d10780c0", 208316672 + 11829760),
+    "mxfp8_8192x65536": ("778e9c37d10780c0", 80143104 + 2087588096),
+    "mxfp4_8192x65536": ("778e9c37d10780c0", 43454720 + 2087773952),
+    "mxfp4_irregular_8192x65536": ("778e9c37d10780c0", 42801664 + 2086061568),
+    "thd_bf16_3seq_8192x32768": ("778e9c37d10780c0", 145014016 + 1012449280),
+}
 
 
 def kernel_source_digest() -> str:
@@ -610,6 +620,24 @@ def run_ours(args, dist):
             "hbm_write_gbs": case.B * case.S * case.N * (2 if args.out_bf16 else 4)
                              / (ms_local * 1e-3) / 1e9 * (flops_rank / flops_total),
             "hbm_peak_gbs": peaks["hbm_gbs"]}
+    # The three floors of one call: tensor (in-window FLOPs at the format's
+    # peak), epilogue FP32 arithmetic (two FP32 lane-ops per in-window
+    # (pair, head) -- the ReLU and the weighted add -- at 128 FP32 lanes per
+    # SM per cycle at the maximum SM clock: the GB300's FP32 throughput), and
+    # HBM (inputs read once plus the logits written once, at the measured copy
+    # rate). The largest is the bound a perfect kernel would meet.
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sm_hz = 1e6 * float((clk or {}).get("sm_max_mhz") or 2070.0)
+    in_bytes = sum(a.nbytes for a in (case.q, case.k, case.w, case.ks, case.ke, case.q_sf,
+                                      case.k_sf, case.k_tok) if a is not None)
+    out_bytes = case.B * case.S * case.N * (2 if args.out_bf16 else 4)
+    floors = {"tensor_us": 1e6 * flops_rank / (peak * 1e12),
+              "epilogue_fp32_us": 1e6 * (flops_rank / (2.0 * case.D)) * 2.0 / (sms * 128 * sm_hz),
+              "hbm_us": 1e6 * (in_bytes + out_bytes) / (peaks["hbm_gbs"] * 1e9)}
+    bound_name = max(floors, key=floors.get)
+    roof["floors"] = floors
+    roof["largest_floor"] = bound_name[:-3]
+    roof["frac_of_largest_floor"] = floors[bound_name] / (1e3 * ms_local / calls_per_step)
     if case.page_size:
         # Decode reads each batch's keys once and is bound by HBM: report
         # the algorithmic bytes (keys up to each batch's longest window with

@@ -280,6 +280,25 @@ IDX_API int indexer_logits_topk(const void* q, const uint8_t* q_sf, const void* 
                                 int64_t idx_stride, void* workspace, int64_t workspace_bytes,
                                 idx_stream_t stream);
 
+/* Windows of sequences packed along the rows and keys of one batch (the
+ * THD / varlen layout: cuDNN-frontend pull request 416, "What" and its THD
+ * commit), computed on the device from cumulative lengths, for a call with
+ * B = 1, S = total_q and N = the packed key count; its logits columns are
+ * then global key positions.
+ *  cu_seqlens_q, cu_seqlens_k  device int32 [num_seqs + 1], non-decreasing,
+ *               starting at 0: sequence s owns rows [cu_q[s], cu_q[s+1]) and
+ *               keys [cu_k[s], cu_k[s+1]).
+ *  causal       non-zero: row r of a sequence with n_q rows and n_k keys sees
+ *               its first clamp(n_k - n_q + r + 1, 0, n_k) keys (the last row
+ *               all of them); zero: all n_k keys.
+ *  ks, ke       device int32 [total_q] written with absolute windows; rows at
+ *               or past cu_q[num_seqs] get the empty window [0, 0).
+ * Asynchronous on `stream`; IDX_ERR_NULL, IDX_ERR_SHAPE (num_seqs or total_q
+ * < 1), IDX_ERR_ALIGN (pointers not 4-byte aligned), IDX_ERR_CUDA. */
+IDX_API int indexer_thd_windows(const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                int32_t num_seqs, int32_t total_q, int32_t causal, int32_t* ks,
+                                int32_t* ke, idx_stream_t stream);
+
 /* Human-readable text for an idx_status value (static storage, never NULL). */
 IDX_API const char* indexer_status_string(int status);
 

@@ -85,6 +85,8 @@ def load():
         lib.indexer_logits_topk.restype = i32
         lib.indexer_logits_topk.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float,
                                             ctypes.POINTER(idx_shape), i32, vp, i64, vp, i64, vp]
+        lib.indexer_thd_windows.restype = i32
+        lib.indexer_thd_windows.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
         lib.indexer_selftest_wait_timeout.restype = i32
         lib.indexer_selftest_wait_timeout.argtypes = [i64, vp]
         lib.indexer_noalloc_get_last_error.restype = i32
@@ -245,6 +247,23 @@ def topk_case(case, t, topk: int, idx=None, workspace=None, stream=None):
     indexer_logits_topk(t["q"], t["q_sf"], t["k"], t["k_sf"], t["k_scales"], t["w"], t["ks"],
                         t["ke"], case.sm_scale, shape, topk, idx, workspace, stream)
     return idx
+
+
+def indexer_thd_windows(cu_seqlens_q, cu_seqlens_k, total_q: int, causal=True, ks=None,
+                        ke=None, stream=None):
+    """Absolute per-row windows of packed sequences from cumulative lengths
+    (int32 CUDA tensors [num_seqs + 1]); returns (ks, ke) int32 [1, total_q]."""
+    dev = cu_seqlens_q.device
+    if ks is None:
+        ks = torch.empty(1, total_q, dtype=torch.int32, device=dev)
+    if ke is None:
+        ke = torch.empty(1, total_q, dtype=torch.int32, device=dev)
+    st = load().indexer_thd_windows(_ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                                    int(cu_seqlens_q.numel() - 1), int(total_q),
+                                    int(bool(causal)), _ptr(ks), _ptr(ke), _stream(stream))
+    if st != IDX_OK:
+        raise IndexerError(st, "indexer_thd_windows")
+    return ks, ke
 
 
 def indexer_selftest_wait_timeout(limit_ns: int, stream=None) -> None:

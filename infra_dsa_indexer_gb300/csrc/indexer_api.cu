@@ -16,6 +16,7 @@
 #include "indexer_kernel.cuh"
 #include "plan_kernel.cuh"
 #include "topk_kernel.cuh"
+#include "window_kernel.cuh"
 
 namespace {
 
@@ -654,6 +655,21 @@ int indexer_logits_topk(const void* q, const uint8_t* q_sf, const void* k, const
     dsa::topk_merge_kernel<kMany><<<grid, kMany, 0, stream>>>(
         smp, ws.ns_cols, static_cast<int>(ws.ns_cols), kept, ws.cap, mask, ws.mask_stride,
         dsa::kSampleEvery, topk, idx, idx_stride);
+  return cudaGetLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+}
+
+int indexer_thd_windows(const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                        int32_t num_seqs, int32_t total_q, int32_t causal, int32_t* ks,
+                        int32_t* ke, idx_stream_t stream_) {
+  if (!cu_seqlens_q || !cu_seqlens_k || !ks || !ke) return IDX_ERR_NULL;
+  if (num_seqs < 1 || total_q < 1) return IDX_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(cu_seqlens_q) | reinterpret_cast<uintptr_t>(cu_seqlens_k) |
+       reinterpret_cast<uintptr_t>(ks) | reinterpret_cast<uintptr_t>(ke)) & 3u)
+    return IDX_ERR_ALIGN;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const unsigned blocks = static_cast<unsigned>((total_q + dsa::kWindowThreads - 1) / dsa::kWindowThreads);
+  dsa::thd_windows_kernel<<<blocks, dsa::kWindowThreads, 0, stream>>>(
+      cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, causal != 0, ks, ke);
   return cudaGetLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }
 

@@ -209,3 +209,17 @@ def test_fused_topk_host_validation(lib, over, status):
                                    ctypes.c_float(0.1), a["shape"], a["topk"], a["idx"],
                                    a["idx_stride"], a["workspace"], a["workspace_bytes"],
                                    None) == status
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(cu_q=None), 1),
+    (dict(ke=None), 1),
+    (dict(num_seqs=0), 2),
+    (dict(total_q=0), 2),
+    (dict(ks=ctypes.c_void_p(0x1002)), 4),
+])
+def test_thd_windows_host_validation(lib, over, status):
+    a = dict(cu_q=FAKE, cu_k=FAKE, num_seqs=3, total_q=10, causal=1, ks=FAKE, ke=FAKE)
+    a.update(over)
+    assert lib.indexer_thd_windows(a["cu_q"], a["cu_k"], a["num_seqs"], a["total_q"],
+                                   a["causal"], a["ks"], a["ke"], None) == status
