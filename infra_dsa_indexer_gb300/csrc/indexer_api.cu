@@ -28,7 +28,9 @@ struct DeviceInfo {
   bool valid = false;
   int sm_count = 0;
   int cc_major = 0, cc_minor = 0;
-  bool smem_set[128] = {};  // per kernel instantiation (format, mode, sign, output type, paging)
+  // per kernel instantiation: format, mode, sign, output type, paging (and,
+  // from 128 on, the two-row-block BF16/E4M3 kernels)
+  bool smem_set[136] = {};
   bool plan_attr_set = false;
 };
 
@@ -160,24 +162,49 @@ int encode_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, in
   return r == CUDA_SUCCESS ? IDX_OK : IDX_ERR_CUDA;
 }
 
-template <int FMT, bool NEG_EPI, bool OUT_BF16, bool PAGED, int MODE = dsa::kModeLogits>
+template <int FMT, bool NEG_EPI, bool OUT_BF16, bool PAGED, int MODE = dsa::kModeLogits,
+          int RB = dsa::kRowsPerBlock>
 int launch_kernel(const KernelParams& prm, int grid, DeviceInfo* di, cudaStream_t stream) {
-  constexpr int smem = dsa::Layout<FMT>::kBytes;
-  auto kern = dsa::indexer_logits_kernel<FMT, NEG_EPI, OUT_BF16, PAGED, MODE>;
-  bool& attr_set = di->smem_set[FMT * 32 + MODE * 8 + (NEG_EPI ? 4 : 0) + (OUT_BF16 ? 2 : 0) +
-                                (PAGED ? 1 : 0)];
+  constexpr int smem = dsa::Layout<FMT, RB>::kBytes;
+  auto kern = dsa::indexer_logits_kernel<FMT, NEG_EPI, OUT_BF16, PAGED, MODE, RB>;
+  static_assert(RB == dsa::kRowsPerBlock || FMT < 2, "two-row blocks: BF16 and E4M3");
+  bool& attr_set =
+      di->smem_set[RB == dsa::kRowsPerBlock
+                       ? FMT * 32 + MODE * 8 + (NEG_EPI ? 4 : 0) + (OUT_BF16 ? 2 : 0) +
+                             (PAGED ? 1 : 0)
+                       : 128 + FMT * 4 + (OUT_BF16 ? 2 : 0) + (PAGED ? 1 : 0)];
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
       return IDX_ERR_CUDA;
     attr_set = true;
   }
-  kern<<<grid, dsa::Layout<FMT>::kThreads, smem, stream>>>(prm);
+  kern<<<grid, dsa::Layout<FMT, RB>::kThreads, smem, stream>>>(prm);
   return cudaGetLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }
 
+// Query rows per block of a call: 2 for BF16/E4M3 logits whose batches have
+// at most two rows (decode), where four-row blocks would leave half of each
+// MMA and of the epilogue warps without a row; else kRowsPerBlock.
+int rows_per_block(const idx_shape& sh, int mode, bool grouped) {
+  const bool two = (sh.fmt == IDX_FMT_BF16 || sh.fmt == IDX_FMT_E4M3) && sh.S <= 2 &&
+                   mode == dsa::kModeLogits && !grouped;
+  return two ? 2 : dsa::kRowsPerBlock;
+}
+
 template <int FMT, bool NEG_EPI>
-int launch(const KernelParams& prm, int grid, DeviceInfo* di, cudaStream_t stream, int mode) {
+int launch(const KernelParams& prm, int grid, DeviceInfo* di, cudaStream_t stream, int mode,
+           int rb) {
+  if constexpr (FMT == dsa::kFmtBF16 || FMT == dsa::kFmtE4M3) {
+    if (rb == 2) {
+      constexpr int kM = dsa::kModeLogits;
+      if (prm.block_table != nullptr)
+        return prm.out_bf16 ? launch_kernel<FMT, false, true, true, kM, 2>(prm, grid, di, stream)
+                            : launch_kernel<FMT, false, false, true, kM, 2>(prm, grid, di, stream);
+      return prm.out_bf16 ? launch_kernel<FMT, false, true, false, kM, 2>(prm, grid, di, stream)
+                          : launch_kernel<FMT, false, false, false, kM, 2>(prm, grid, di, stream);
+    }
+  }
   if (mode == dsa::kModeSample)
     return launch_kernel<FMT, NEG_EPI, false, false, dsa::kModeSample>(prm, grid, di, stream);
   if (mode == dsa::kModeFilter)
@@ -371,7 +398,8 @@ int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
   prm.w_bf16 = sh.w_fmt == IDX_W_BF16;
   prm.clean = clean != 0 || pass.mode == dsa::kModeSample;
   prm.sm_scale = sm_scale;
-  prm.blocks_per_batch = (sh.S + dsa::kRowsPerBlock - 1) / dsa::kRowsPerBlock;
+  const int rb = rows_per_block(sh, pass.mode, groups_rows(sh, fixed_scratch));
+  prm.blocks_per_batch = (sh.S + rb - 1) / rb;
   prm.timeout_ns = static_cast<uint64_t>(g_wait_limit_ns);
 
   // Units: every row-block split into nchunk pieces of its key tiles. Long
@@ -397,12 +425,12 @@ int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
 
   const int mode = pass.mode;
   switch (sh.fmt) {
-    case IDX_FMT_BF16: return launch<dsa::kFmtBF16, false>(prm, grid, di, stream, mode);
-    case IDX_FMT_E4M3: return launch<dsa::kFmtE4M3, false>(prm, grid, di, stream, mode);
-    case IDX_FMT_MXFP8: return launch<dsa::kFmtMXFP8, false>(prm, grid, di, stream, mode);
+    case IDX_FMT_BF16: return launch<dsa::kFmtBF16, false>(prm, grid, di, stream, mode, rb);
+    case IDX_FMT_E4M3: return launch<dsa::kFmtE4M3, false>(prm, grid, di, stream, mode, rb);
+    case IDX_FMT_MXFP8: return launch<dsa::kFmtMXFP8, false>(prm, grid, di, stream, mode, rb);
     case IDX_FMT_MXFP4:
-      return sm_scale < 0.f ? launch<dsa::kFmtMXFP4, true>(prm, grid, di, stream, mode)
-                            : launch<dsa::kFmtMXFP4, false>(prm, grid, di, stream, mode);
+      return sm_scale < 0.f ? launch<dsa::kFmtMXFP4, true>(prm, grid, di, stream, mode, rb)
+                            : launch<dsa::kFmtMXFP4, false>(prm, grid, di, stream, mode, rb);
     default: return IDX_ERR_UNSUPPORTED;
   }
 }

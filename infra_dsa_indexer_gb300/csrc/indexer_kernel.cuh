@@ -161,7 +161,7 @@ struct KernelParams {
   int32_t clean;
   int32_t num_units;
   int32_t nchunk;
-  int32_t blocks_per_batch;  // ceil(S / 4); the last block of a batch may be partial
+  int32_t blocks_per_batch;  // ceil(S / rows per block); the last block may be partial
   float sm_scale;
   uint64_t timeout_ns;
 };
@@ -231,21 +231,33 @@ struct Traits<kFmtMXFP4> {
   static constexpr bool kReluAllAdd = true;  // packed-add ReLU on every head pair (RowAcc)
 };
 
-template <int FMT>
+// RB: query rows per block, kRowsPerBlock, or 2 for batches of at most two
+// rows (decode with one or two new tokens), where a four-row block would
+// leave half of every MMA and of the epilogue warps without a row. With
+// RB = 2 the MMA is N = 128 into four 128-column accumulators and the
+// epilogue warps form two groups that take alternate tiles (BF16 and E4M3;
+// the MX formats keep one accumulator and RB = 4).
+template <int FMT, int RB = kRowsPerBlock>
 struct Layout {
   using T = Traits<FMT>;
+  static_assert(RB == kRowsPerBlock || (RB == 2 && !T::kMX), "rows per block");
   static constexpr int kNumEpiWarps = 4 * kRowsPerBlock / T::kRowsPerWarp;
   static constexpr int kThreads = (kEpiWarp0 + kNumEpiWarps) * 32;
-  static constexpr int kAccBufs = T::kMX ? 1 : 2;
+  static constexpr int kBlockNR = RB * kHeads;                    // MMA N
+  static constexpr int kGroups = kRowsPerBlock / RB;              // epilogue warp groups
+  static constexpr int kGroupWarps = kNumEpiWarps / kGroups;
+  static constexpr int kAccBufs = T::kMX ? 1 : 2 * kGroups;       // accumulators of kBlockNR columns
+  // The instruction descriptor with its N field (bits [17,23), N >> 3) set to kBlockNR.
+  static constexpr uint32_t kIdesc = (T::kIdesc & ~(0x3Fu << 17)) | ((kBlockNR >> 3) << 17);
   static constexpr int kPanels = T::kRowBytes / T::kSwizzleBytes;
   static constexpr int kSteps = T::kRowBytes / kStepBytes;           // MMAs per tile
   static constexpr int kStepsPerPanel = T::kSwizzleBytes / kStepBytes;
   static constexpr int kAtomBytes = 8 * T::kSwizzleBytes;            // 8-row swizzle atom
   static constexpr int kKPanelBytes = kKeysPerTile * T::kSwizzleBytes;
-  static constexpr int kQPanelBytes = kBlockN * T::kSwizzleBytes;
+  static constexpr int kQPanelBytes = kBlockNR * T::kSwizzleBytes;
   static constexpr int kKTileBytes = kKPanelBytes * kPanels;
   static constexpr int kQBlockBytes = kQPanelBytes * kPanels;
-  static constexpr int kWBytes = kRowsPerBlock * kHeads * 4;  // FP32 weights of a block
+  static constexpr int kWBytes = RB * kHeads * 4;  // FP32 weights of a block
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + 2 * kQBlockBytes;
   static constexpr int kWOff = kKOff + T::kStages * kKTileBytes;
@@ -369,12 +381,15 @@ __device__ __forceinline__ void mma_step(uint32_t d_tmem, uint64_t a_desc, uint6
 // OUT_BF16: the logits are stored as BF16 (round to nearest even).
 // PAGED: the keys (and key scales) are read through the page table.
 // MODE: kModeLogits, or one of the two passes of the fused top-k call.
-template <int FMT, bool NEG_EPI, bool OUT_BF16, bool PAGED, int MODE = kModeLogits>
-__global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
+// RB: rows per block (Layout).
+template <int FMT, bool NEG_EPI, bool OUT_BF16, bool PAGED, int MODE = kModeLogits,
+          int RB = kRowsPerBlock>
+__global__ void __launch_bounds__(Layout<FMT, RB>::kThreads, 1)
     indexer_logits_kernel(const __grid_constant__ KernelParams p) {
   static_assert(MODE == kModeLogits || (!OUT_BF16 && !PAGED), "fused top-k: FP32, contiguous keys");
+  static_assert(RB == kRowsPerBlock || MODE == kModeLogits, "fused top-k: four-row blocks");
   using T = Traits<FMT>;
-  using L = Layout<FMT>;
+  using L = Layout<FMT, RB>;
   constexpr int kNumEpiWarps = L::kNumEpiWarps;
   constexpr int kAccBufs = L::kAccBufs;
   constexpr int R = T::kRowsPerWarp;
@@ -424,7 +439,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
     }
     for (int s = 0; s < kAccBufs; ++s) {
       mbar_init(&acc_full[s], 1);
-      mbar_init(&acc_empty[s], kNumEpiWarps);
+      mbar_init(&acc_empty[s], L::kGroupWarps);  // the warps of the group that drains it
     }
     for (int s = 0; s < T::kStages; ++s) {
       mbar_init(&k_full[s], 1);
@@ -483,20 +498,21 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       q.chunk = u - order * p.nchunk;
       q.blk = p.blocks_per_batch - 1 - order / p.B;
       q.b = order % p.B;
-      // The block's rows: positions 4*blk .. 4*blk+3 of the batch's row
+      // The block's rows: positions RB*blk .. RB*blk+RB-1 of the batch's row
       // order. Positions past S (a partial last block) read the batch's last
       // row in that order, so every address stays valid; the row gets an
-      // empty window and is never stored.
+      // empty window and is never stored. With RB = 2, rows 2 and 3 of the
+      // unit info are absent and their addresses are those of row 0.
 #pragma unroll
       for (int r = 0; r < kRowsPerBlock; ++r) {
-        const int pos = min(q.blk * kRowsPerBlock + r, p.S - 1);
+        const int pos = min(q.blk * RB + (r < RB ? r : 0), p.S - 1);
         q.grow[r] = q.b * p.S + (p.perm != nullptr ? __ldg(p.perm + q.b * p.S + pos) : pos);
       }
       if (lane == 0) {
         int lo_all = p.N, hi_all = 0;
 #pragma unroll
         for (int r = 0; r < kRowsPerBlock; ++r) {
-          const bool exists = q.blk * kRowsPerBlock + r < p.S;
+          const bool exists = r < RB && q.blk * RB + r < p.S;
           const int lo = exists ? clampi(__ldg(p.ks + q.grow[r]), 0, p.N) : 0;
           const int hi = exists ? clampi(__ldg(p.ke + q.grow[r]), 0, p.N) : 0;
           q.in.row[r] = exists ? q.grow[r] : -1;
@@ -522,9 +538,11 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         q.in.flags = (q.chunk == 0 ? 1 : 0) | (q.chunk == p.nchunk - 1 ? 2 : 0);
       }
       if (p.w_bf16) {
-        // lane l: 8 weights = 16 bytes, row l/8, heads 8*(l%8)..
+        // lane l: 8 weights = 16 bytes, row l/8, heads 8*(l%8).. (rows past
+        // RB: row 0 again, not stored)
         const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.w) +
-                                static_cast<int64_t>(pick(q.grow, lane >> 3)) * (kHeads / 8) +
+                                static_cast<int64_t>(pick(q.grow, (lane >> 3) % RB)) *
+                                    (kHeads / 8) +
                                 (lane & 7));
         q.w[0] = make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u),
                              __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u));
@@ -534,7 +552,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         // float4 f = lane + 32i: row f/16, heads 4*(f%16)..
         const float4* src = reinterpret_cast<const float4*>(p.w);
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < RB / 2; ++i) {
           const int f = lane + 32 * i;
           q.w[i] = __ldg(src + static_cast<int64_t>(pick(q.grow, f >> 4)) * (kHeads / 4) + (f & 15));
         }
@@ -606,7 +624,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
           // the block (a whole number of swizzle atoms).
           uint8_t* qdst = qbuf + slot * L::kQBlockBytes;
 #pragma unroll
-          for (int r = 0; r < kRowsPerBlock; ++r)
+          for (int r = 0; r < RB; ++r)
 #pragma unroll
             for (int pnl = 0; pnl < L::kPanels; ++pnl)
               tma_load_2d(qdst + pnl * L::kQPanelBytes + r * kHeads * T::kSwizzleBytes,
@@ -630,32 +648,57 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       // Epilogue half: free once the epilogue is done with unit it-2.
       if (!wait_half(unit_empty, it, it > 1 ? it - 1 : 0, it + 1)) break;
       if (lane == 0) in = cur.in;
-      // Head weights of the 4 rows as FP32, row-major 4 x 64.
+      // Head weights of the RB rows as FP32, row-major RB x 64.
       float4* wdst = reinterpret_cast<float4*>(wbuf + slot * L::kWBytes);
       if (p.w_bf16) {
-        wdst[2 * lane] = cur.w[0];
-        wdst[2 * lane + 1] = cur.w[1];
+        if (lane < 8 * RB) {
+          wdst[2 * lane] = cur.w[0];
+          wdst[2 * lane + 1] = cur.w[1];
+        }
       } else {
-        wdst[lane] = cur.w[0];
-        wdst[lane + 32] = cur.w[1];
+#pragma unroll
+        for (int i = 0; i < RB / 2; ++i) wdst[lane + 32 * i] = cur.w[i];
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&unit_full[slot]);
       if (ahead) prepare(__shfl_sync(0xffffffffu, u_next, 0), cur);
     }
-  } else if (warp == 0 && (T::kMX || lane == 0)) {
+  } else if (warp == 0 && (T::kMX || PAGED || lane == 0)) {
     // ------------------------------------------------------- K-tile producer
     // Lane 0 waits and issues the TMA; for MX formats all lanes also copy the
     // tile's 128 key scale words (word of key m = 32c + lane to row `lane`,
-    // word c of the 16-byte rows the TMEM copy reads).
+    // word c of the 16-byte rows the TMEM copy reads); for paged keys all
+    // lanes hold block-table entries (page_entry).
+    constexpr bool kWarpWide = T::kMX || PAGED;
     if (lane == 0) prefetch_tmap(&p.tmap_k);
     const uint64_t pol_k = policy_evict_last();  // K is re-read by every row-block
+    // Paged keys: the unit's table entries, 32 per load, lane l holding
+    // entry `win` + l (`cur`) and `win` + 32 + l (`nxt`). The next 32 are
+    // requested on entering a window, so the table's latency is spread over
+    // the tiles of 32 entries instead of stalling every TMA issue.
+    const int n_entries = PAGED ? (p.N + p.page_size - 1) / p.page_size : 0;
+    const int32_t* table = nullptr;
+    int win = 0, cur = 0, nxt = 0;
+    auto fetch_entry = [&](int e) { return e < n_entries ? __ldg(table + e) : 0; };
+    auto page_entry = [&](int e) {  // warp-collective; e warp-uniform, e >= win
+      if (e >= win + 32) {
+        if (e < win + 64) {
+          cur = nxt;
+          win += 32;
+        } else {
+          win = e;
+          cur = fetch_entry(win + lane);
+        }
+        nxt = fetch_entry(win + 32 + lane);
+      }
+      return clampi(__shfl_sync(0xffffffffu, cur, e - win), 0, p.num_pages - 1);
+    };
     uint32_t kiter = 0;
     for (uint32_t it = 0;; ++it) {
       const int slot = it & 1;
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&q_full[slot], (it >> 1) & 1, abort_flag, p.timeout_ns);
-      if constexpr (T::kMX) {
+      if constexpr (kWarpWide) {
         ok = __shfl_sync(0xffffffffu, ok, 0);
         __syncwarp();  // lane 0's acquire covers the QInfo the other lanes read
       }
@@ -668,11 +711,29 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       const QInfo& qi = qinfo[slot];
       if (qi.stop) break;
       const int c0 = qi.c0, c1 = qi.c1, b = qi.b;
+      if constexpr (PAGED) {
+        table = p.block_table + static_cast<int64_t>(b) * p.table_stride;
+        win = c0 * kKeysPerTile / p.page_size;
+        cur = fetch_entry(win + lane);
+        nxt = fetch_entry(win + 32 + lane);
+      }
       for (int t = first_tile<MODE>(c0); t < c1; t = next_tile<MODE>(t), ++kiter) {
         const int st = kiter % T::kStages;
+        // Rows of the tile's two 64-key boxes, each inside one page (page_size
+        // is a multiple of 64). The first box starts below N; a second box
+        // wholly past N re-reads the first one's rows (keys no window reads).
+        int prow[2] = {0, 0};
+        if constexpr (PAGED) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int k0 = t * kKeysPerTile + 64 * h;
+            prow[h] = k0 < p.N ? page_entry(k0 / p.page_size) * p.page_size + k0 % p.page_size
+                               : prow[0];
+          }
+        }
         if (lane == 0)
           ok = mbar_wait(&k_empty[st], ((kiter / T::kStages) & 1) ^ 1, abort_flag, p.timeout_ns);
-        if constexpr (T::kMX) ok = __shfl_sync(0xffffffffu, ok, 0);
+        if constexpr (kWarpWide) ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(&k_full[st], L::kKTileBytes);
@@ -683,19 +744,13 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
               tma_load_3d(kdst + pnl * L::kKPanelBytes, &p.tmap_k, &k_full[st],
                           pnl * (T::kSwizzleBytes / T::kTmaElemBytes), t * kKeysPerTile, b, pol_k);
           } else {
-            // Paged: two 64-key boxes, each inside one page (page_size is a
-            // multiple of 64). A box wholly past N loads the page of key 0
-            // (rows no window reads) so that no table entry past the
-            // batch's keys is used.
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int k0 = t * kKeysPerTile + 64 * h;
-              const int prow = static_cast<int>(key_row<PAGED>(p, b, k0 < p.N ? k0 : 0));
+            for (int h = 0; h < 2; ++h)
 #pragma unroll
               for (int pnl = 0; pnl < L::kPanels; ++pnl)
                 tma_load_2d(kdst + pnl * L::kKPanelBytes + h * 64 * T::kSwizzleBytes, &p.tmap_k,
-                            &k_full[st], pnl * (T::kSwizzleBytes / T::kTmaElemBytes), prow, pol_k);
-            }
+                            &k_full[st], pnl * (T::kSwizzleBytes / T::kTmaElemBytes), prow[h],
+                            pol_k);
           }
         }
         if constexpr (T::kMX) {
@@ -737,7 +792,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
     uint32_t kiter = 0, aiter = 0, units_mma = 0;
     // ReLU(s*x) = |s| * max(-x, 0) for s < 0: negate the A operand (bit 13),
     // except where the epilogue applies the sign (NEG_EPI).
-    const uint32_t idesc = T::kIdesc | (!NEG_EPI && p.sm_scale < 0.f ? (1u << 13) : 0u);
+    const uint32_t idesc = L::kIdesc | (!NEG_EPI && p.sm_scale < 0.f ? (1u << 13) : 0u);
     // K-major operands, 8-row groups one swizzle atom apart; layout code
     // 2 = 128-byte swizzle, 4 = 64-byte swizzle.
     constexpr uint32_t kLayout = T::kSwizzleBytes == 128 ? 2u : 4u;
@@ -803,7 +858,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         // Descriptors differ only in the start-address field (bits 0-13,
         // address >> 4), so every step is the stage/slot base plus an offset.
         const uint64_t a_base = k_desc0 + ((st * L::kKTileBytes) >> 4);
-        const uint32_t d_tmem = tmem_base + acc * kBlockN;
+        const uint32_t d_tmem = tmem_base + acc * L::kBlockNR;
 #pragma unroll
         for (int kk = 0; kk < L::kSteps; ++kk) {
           const uint32_t pnl = kk / L::kStepsPerPanel, step = kk % L::kStepsPerPanel;
@@ -834,8 +889,13 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
     }
   } else if (warp >= kEpiWarp0) {
     // ---------------------------------------------------------------- epilogue
-    const int quarter = warp & 3;                  // TMEM sub-partition of this warp
-    const int r0 = R * ((warp - kEpiWarp0) >> 2);  // rows r0 .. r0 + R - 1 of the block
+    const int quarter = warp & 3;  // TMEM sub-partition of this warp
+    // Groups of warps (one with RB = 4) take alternate tiles: group g the
+    // tiles whose index over all units (aiter) is g mod kGroups.
+    constexpr int kGroups = L::kGroups;
+    constexpr int kWarpRows = RB / R;  // warps per sub-partition in a group
+    const int grp = ((warp - kEpiWarp0) >> 2) / kWarpRows;
+    const int r0 = R * (((warp - kEpiWarp0) >> 2) % kWarpRows);  // rows r0 .. r0 + R - 1
     const int tid128 = quarter * 32 + lane;        // index among the rows' 4 warps
     // The MMA delivers x = s_sign * q.k (negated A for s < 0), so the sum is
     // scaled by |s|; with NEG_EPI the epilogue sums min(x, 0) and scales by s.
@@ -879,7 +939,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
       const float* wrows = reinterpret_cast<const float*>(wbuf + slot * L::kWBytes) + r0 * kHeads;
       // Compact sample column of the first key of tile t (kModeSample).
       auto sample_col = [](int t) { return first_tile<kModeSample>(t) / kSampleEvery * kKeysPerTile; };
-      if (p.clean && (flags & 1) && MODE != kModeFilter) {
+      if (p.clean && (flags & 1) && MODE != kModeFilter && grp == 0) {
         const int end = MODE == kModeSample ? sample_col(t0) : t0 * kKeysPerTile;
 #pragma unroll
         for (int r = 0; r < R; ++r)
@@ -909,9 +969,12 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         const int jj = t * kKeysPerTile + quarter * 32 + lane;
         return __ldg(p.k_scales + static_cast<int64_t>(page) * p.page_size + jj % p.page_size);
       };
-      int page_ahead = PAGED ? load_page(c0 + 1) : -1;
-      float kscale_next =
-          PAGED ? scale_in_page(c0, load_page(c0)) : load_kscale(first_tile<MODE>(c0));
+      // This group's first tile of the unit; its later ones are kGroups
+      // apart (kGroups > 1 only computes logits, where tiles are consecutive).
+      const int tf = first_tile<MODE>(c0) +
+                     (kGroups > 1 ? static_cast<int>((grp + kGroups - aiter % kGroups) % kGroups) : 0);
+      int page_ahead = PAGED ? load_page(tf + kGroups) : -1;
+      float kscale_next = PAGED ? scale_in_page(tf, load_page(tf)) : load_kscale(tf);
       bool ok = true;
       if (PAGED && !any_row) {
         // Every row of this warp is past S (a partial last block; decode with
@@ -920,6 +983,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         // the E4M3 tile loop, and there the absent rows are just computed
         // and not stored.
         for (int t = c0; t < c1; ++t, ++aiter) {
+          if (kGroups > 1 && static_cast<int>(aiter % kGroups) != grp) continue;
           if (!mbar_wait(&acc_full[aiter % kAccBufs], (aiter / kAccBufs) & 1, abort_flag,
                          p.timeout_ns)) {
             ok = false;
@@ -930,14 +994,15 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         }
       } else {
         for (int t = first_tile<MODE>(c0); t < c1; t = next_tile<MODE>(t), ++aiter) {
+          if (kGroups > 1 && static_cast<int>(aiter % kGroups) != grp) continue;
           const int acc = aiter % kAccBufs;
           const int j = t * kKeysPerTile + quarter * 32 + lane;
           const float kscale = kscale_next;
           if constexpr (PAGED) {
-            kscale_next = scale_in_page(t + 1, page_ahead);
-            page_ahead = load_page(t + 2);
+            kscale_next = scale_in_page(t + kGroups, page_ahead);
+            page_ahead = load_page(t + 2 * kGroups);
           } else {
-            kscale_next = load_kscale(next_tile<MODE>(t));
+            kscale_next = load_kscale(kGroups > 1 ? t + kGroups : next_tile<MODE>(t));
           }
           if (!mbar_wait(&acc_full[acc], (aiter / kAccBufs) & 1, abort_flag, p.timeout_ns)) {
             ok = false;
@@ -947,7 +1012,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
           __syncwarp();  // tcgen05.ld is warp-collective: converge first
           // Read the rows' 64 columns each, hand the accumulator back, reduce.
           const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                 acc * kBlockN + r0 * kHeads;
+                                 acc * L::kBlockNR + r0 * kHeads;
           uint32_t v[R][64];
           RowAcc<NEG_EPI, T::kReluAllAdd> racc[R];
 #pragma unroll
@@ -1004,7 +1069,7 @@ __global__ void __launch_bounds__(Layout<FMT>::kThreads, 1)
         raise_error(p.scratch, abort_flag, kErrTimeout);
         break;
       }
-      if (p.clean && (flags & 2) && MODE != kModeFilter) {
+      if (p.clean && (flags & 2) && MODE != kModeFilter && grp == 0) {
         const int from = MODE == kModeSample ? sample_col(t1) : t1 * kKeysPerTile;
         const int to = MODE == kModeSample ? static_cast<int>(p.out_row_stride) : p.N;
 #pragma unroll
