@@ -541,7 +541,9 @@ __global__ void __launch_bounds__(Layout<FMT, RB>::kThreads, 1)
         // lane l: 8 weights = 16 bytes, row l/8, heads 8*(l%8).. (rows past
         // RB: row 0 again, not stored)
         const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.w) +
-                                static_cast<int64_t>(pick(q.grow, (lane >> 3) % RB)) *
+                                static_cast<int64_t>(pick(q.grow, RB == kRowsPerBlock
+                                                                      ? lane >> 3
+                                                                      : (lane >> 3) % RB)) *
                                     (kHeads / 8) +
                                 (lane & 7));
         q.w[0] = make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u),
@@ -651,7 +653,7 @@ __global__ void __launch_bounds__(Layout<FMT, RB>::kThreads, 1)
       // Head weights of the RB rows as FP32, row-major RB x 64.
       float4* wdst = reinterpret_cast<float4*>(wbuf + slot * L::kWBytes);
       if (p.w_bf16) {
-        if (lane < 8 * RB) {
+        if (RB == kRowsPerBlock || lane < 8 * RB) {
           wdst[2 * lane] = cur.w[0];
           wdst[2 * lane + 1] = cur.w[1];
         }
@@ -892,10 +894,13 @@ __global__ void __launch_bounds__(Layout<FMT, RB>::kThreads, 1)
     const int quarter = warp & 3;  // TMEM sub-partition of this warp
     // Groups of warps (one with RB = 4) take alternate tiles: group g the
     // tiles whose index over all units (aiter) is g mod kGroups.
+    // (Both are compile-time constants with one group, so the four-row
+    // kernels keep no extra live register in their tile loop.)
     constexpr int kGroups = L::kGroups;
     constexpr int kWarpRows = RB / R;  // warps per sub-partition in a group
-    const int grp = ((warp - kEpiWarp0) >> 2) / kWarpRows;
-    const int r0 = R * (((warp - kEpiWarp0) >> 2) % kWarpRows);  // rows r0 .. r0 + R - 1
+    const int wrow = (warp - kEpiWarp0) >> 2;
+    const int grp = kGroups > 1 ? wrow / kWarpRows : 0;
+    const int r0 = R * (kGroups > 1 ? wrow % kWarpRows : wrow);  // rows r0 .. r0 + R - 1
     const int tid128 = quarter * 32 + lane;        // index among the rows' 4 warps
     // The MMA delivers x = s_sign * q.k (negated A for s < 0), so the sum is
     // scaled by |s|; with NEG_EPI the epilogue sums min(x, 0) and scales by s.
