@@ -64,15 +64,15 @@ KERNEL_FILES = ("indexer_kernel.cuh", "ptx.cuh", "plan_kernel.cuh")
 # DRAM bytes (read + write) of one logits-kernel launch from an ncu capture,
 # keyed by workload, with the kernel-source digest it was taken on.
 PROFILED_TRAFFIC = {
-    "bf16_batched_causal_4096": ("778e9c37d10780c0", 137480960 + 79307008),
-    "fp8_per_token_2048x32768": ("778e9c37d10780c0", 21691648 + 207704576),
-    "mxfp8_2048x32768": ("778e9c37d10780c0", 22223360 + 207711232),
-    "mxfp4_2048x32768": ("778e9c37d10780c0", 11789056 + 207355648),
-    "paged_fp8_decode_64x2_32768": ("778e9c37d10780c0", 208316672 + 11829760),
-    "mxfp8_8192x65536": ("778e9c37d10780c0", 80143104 + 2087588096),
-    "mxfp4_8192x65536": ("778e9c37d10780c0", 43454720 + 2087773952),
-    "mxfp4_irregular_8192x65536": ("778e9c37d10780c0", 42801664 + 2086061568),
-    "thd_bf16_3seq_8192x32768": ("778e9c37d10780c0", 145014016 + 1012449280),
+    "bf16_batched_causal_4096": ("d7e1b03e28308141", 137481984 + 79249664),
+    "fp8_per_token_2048x32768": ("d7e1b03e28308141", 21762304 + 207533824),
+    "mxfp8_2048x32768": ("d7e1b03e28308141", 22235648 + 207523584),
+    "mxfp4_2048x32768": ("d7e1b03e28308141", 11734528 + 206791936),
+    "paged_fp8_decode_64x2_32768": ("d7e1b03e28308141", 208275712 + 12861696),
+    "mxfp8_8192x65536": ("d7e1b03e28308141", 80272384 + 2087801600),
+    "mxfp4_8192x65536": ("d7e1b03e28308141", 42514432 + 2087575808),
+    "mxfp4_irregular_8192x65536": ("d7e1b03e28308141", 42597376 + 2086342400),
+    "thd_bf16_3seq_8192x32768": ("d7e1b03e28308141", 144943360 + 1012995584),
 }
 
 
