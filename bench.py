@@ -76,6 +76,27 @@ PROFILED_TRAFFIC = {
 }
 
 
+def host_cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or the machine type."""
+    import platform
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
 def kernel_source_digest() -> str:
     """Digest of the sources that define the logits kernel."""
     import hashlib
@@ -301,7 +322,7 @@ def run_reference(args, _dist):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(case, args),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nth, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "cpu_model": host_cpu_model()},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -666,7 +687,8 @@ def run_ours(args, dist):
     cpu = None
     if not args.no_cpu_baseline:
         v, cores, desc = oracle_sample_rate(case, args.cpu_seconds)
-        cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc,
+               "cpu_model": host_cpu_model()}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": dist.world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
