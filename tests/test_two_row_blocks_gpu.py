@@ -9,8 +9,8 @@ arithmetic as in a four-row block, so the bars are:
   rows placed first in a batch of three rows, whose third row differs);
 - the float64 oracle on every row;
 
-on contiguous and paged keys, FP32 and BF16 logits, ragged, empty, inverted
-and decode windows, and many short units, so that the alternation of the two
+on contiguous and paged keys, FP32 and BF16 logits, FP32 and BF16 weights,
+ragged, empty, inverted and decode windows, and many short units, so that the alternation of the two
 groups crosses unit boundaries after odd and even tile counts.
 """
 import dataclasses
@@ -81,6 +81,21 @@ def test_two_row_blocks_bitwise_and_oracle(fmt, S, page_size, out_bf16):
     ref, den = oracle_rows(case)
     compare(two.reshape(-1, N).float().cpu().numpy(), ref, den,
             out_rounding=BF16_OUT_ROUNDING if out_bf16 else 0.0, label=f"S={S}")
+
+
+@pytest.mark.parametrize("S", [1, 2])
+@pytest.mark.parametrize("fmt", TWO_ROW)
+def test_two_row_blocks_bf16_weights(fmt, S):
+    # BF16 head weights: only the lanes that hold the block's rows store them.
+    B, N = 30, 1500
+    ks, ke = ragged(B, 3, N, seed=750 + 10 * fmt + S)
+    wide = synth.make_case(fmt, B, 3, N, seed=760 + fmt, ks=ks, ke=ke, w_fmt=synth.W_BF16)
+    case = first_rows(wide, S)
+    two = logits(case)
+    four = logits(wide)[:, :S]
+    assert torch.equal(two.view(torch.int32), four.contiguous().view(torch.int32))
+    ref, den = oracle_rows(case)
+    compare(two.reshape(-1, N).cpu().numpy(), ref, den)
 
 
 @pytest.mark.parametrize("page_size", [64, 256])
