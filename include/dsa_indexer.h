@@ -242,7 +242,8 @@ IDX_API int indexer_topk(const void* logits, int logits_bf16, int64_t rows, int3
  * (as much as the FP32 logits would take), i.e. per row 4 bytes for each key
  * (the sampled logits of one 128-key tile in four, a value slot for each key
  * of the other tiles, so that no input can overflow it) and a mask word per
- * 32 keys of the other tiles. Only kept values are written to the slots. */
+ * 32 keys of the other tiles. Only kept values are written to the slots
+ * (packed at the front of each 32-key group). */
 IDX_API int64_t indexer_logits_topk_workspace_bytes(const idx_shape* shape);
 
 /* The indexer's logits reduced straight to each row's top-k key columns, the
@@ -259,8 +260,8 @@ IDX_API int64_t indexer_logits_topk_workspace_bytes(const idx_shape* shape);
  * How: a first pass computes the logits of every fourth 128-key tile into
  * the workspace; the topk-th largest of them is a lower bound T of the row's
  * topk-th largest logit (those topk values are logits of the row); a second
- * pass over the other tiles keeps only in-window logits >= T (at their own
- * slots in the workspace, with a bit mask per 32 keys); a last selection
+ * pass over the other tiles keeps only in-window logits >= T (packed per 32
+ * keys in the workspace, with a bit mask per 32 keys); a last selection
  * takes the top-k of the sampled logits and the kept values. Five launches on `stream` (six with
  * IDX_FLAG_GROUP_ROWS), no synchronisation, no host read of device data.
  *

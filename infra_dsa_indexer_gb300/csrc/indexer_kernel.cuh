@@ -1058,16 +1058,20 @@ __global__ void __launch_bounds__(Layout<FMT, RB>::kThreads, 1)
               }
             }
           } else {
-            // Keep the in-window values >= the row's threshold at their own
-            // slots, and the group's mask word (no atomics: slots and word
-            // belong to this (row, tile, quarter) alone).
+            // Keep the in-window values >= the row's threshold, packed at the
+            // front of the group's 32 slots in key order (the value of the
+            // key of mask bit l is at the rank of bit l among the set bits),
+            // and the group's mask word; no atomics: slots and word belong
+            // to this (row, tile, quarter) alone. Packing lets the merge read
+            // one sector per group instead of most of the group's line.
             const int grp = (t - t / kSampleEvery - 1) * 4 + quarter;
 #pragma unroll
             for (int r = 0; r < R; ++r) {
               const float v = sums[r] * (sm_abs * kscale);
               const bool pass = rowid[r] >= 0 && j < p.N && j >= lo[r] && j < hi[r] && v >= thr[r];
               const uint32_t m = __ballot_sync(0xffffffffu, pass);
-              if (pass) reinterpret_cast<float*>(orow[r])[grp * 32 + lane] = v;
+              if (pass)
+                reinterpret_cast<float*>(orow[r])[grp * 32 + __popc(m & ((1u << lane) - 1u))] = v;
               if (lane == 0 && m != 0u)
                 p.mask[static_cast<int64_t>(rowid[r]) * p.mask_row_stride + grp] = m;
             }

@@ -248,11 +248,15 @@ struct MergeRow {
     const int tile = (r / per) * sample_every + r % per + 1;
     return tile * 128 + (g & 3) * 32 + l;
   }
+  // A group's kept values are packed at the front of its 32 slots in key
+  // order: the value of mask bit l is at slot popc(mask & (2^l - 1)).
   __device__ __forceinline__ uint32_t key(int e) const {
     if (e < ns) return order_key(__float_as_uint(__ldg(s + e)));
     const int i = e - ns;
-    return (__ldg(mask + (i >> 5)) >> (i & 31)) & 1u
-               ? order_key(__float_as_uint(__ldg(kept + i)))
+    const uint32_t m = __ldg(mask + (i >> 5));
+    return (m >> (i & 31)) & 1u
+               ? order_key(__float_as_uint(
+                     __ldg(kept + (i & ~31) + __popc(m & ((1u << (i & 31)) - 1u)))))
                : 0u;
   }
   __device__ __forceinline__ int col(int e) const {
@@ -262,22 +266,28 @@ struct MergeRow {
   __device__ __forceinline__ void for_each(F&& f) const {
     for_each_key<NT, false>(reinterpret_cast<const char*>(s), ns,
                             [&](int e, uint32_t key) { f(sample_col(e), key); });
-    // A warp takes 32 groups at a time: lane l reads mask word g0 + l, then
-    // every lane loads its slot of each of the 32 groups where that slot is
-    // set (32 independent loads in flight), then visits them.
+    // A warp takes 32 groups at a time: lane l reads mask word g0 + l; then,
+    // eight groups at a time (eight independent loads in flight, within the
+    // 32 registers of a thread at four CTAs per SM), every lane whose bit is
+    // set in a group loads that key's packed slot (the group's first
+    // sectors), then visits them.
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t below = (1u << lane) - 1u;
     for (int g0 = warp * 32; g0 < ngroups; g0 += NT) {
       const uint32_t mw = g0 + lane < ngroups ? __ldg(mask + g0 + lane) : 0u;
-      float v[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const uint32_t m = __shfl_sync(0xffffffffu, mw, i);
-        v[i] = (m >> lane) & 1u ? __ldg(kept + (g0 + i) * 32 + lane) : 0.f;
-      }
+      for (int c = 0; c < 32; c += 8) {
+        float v[8];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const uint32_t m = __shfl_sync(0xffffffffu, mw, i);
-        if ((m >> lane) & 1u) f(kept_col(g0 + i, lane), order_key(__float_as_uint(v[i])));
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t m = __shfl_sync(0xffffffffu, mw, c + i);
+          v[i] = (m >> lane) & 1u ? __ldg(kept + (g0 + c + i) * 32 + __popc(m & below)) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t m = __shfl_sync(0xffffffffu, mw, c + i);
+          if ((m >> lane) & 1u) f(kept_col(g0 + c + i, lane), order_key(__float_as_uint(v[i])));
+        }
       }
     }
   }
