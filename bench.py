@@ -64,15 +64,15 @@ KERNEL_FILES = ("indexer_kernel.cuh", "ptx.cuh", "plan_kernel.cuh")
 # DRAM bytes (read + write) of one logits-kernel launch from an ncu capture,
 # keyed by workload, with the kernel-source digest it was taken on.
 PROFILED_TRAFFIC = {
-    "bf16_batched_causal_4096": ("cd4c5434cfa8448d", 137481728 + 79343872),
-    "fp8_per_token_2048x32768": ("cd4c5434cfa8448d", 21746944 + 207263232),
-    "mxfp8_2048x32768": ("cd4c5434cfa8448d", 22222080 + 207436800),
-    "mxfp4_2048x32768": ("cd4c5434cfa8448d", 11735808 + 207371520),
-    "paged_fp8_decode_64x2_32768": ("cd4c5434cfa8448d", 208150016 + 8081152),
-    "mxfp8_8192x65536": ("cd4c5434cfa8448d", 80089088 + 2087469568),
-    "mxfp4_8192x65536": ("cd4c5434cfa8448d", 42767872 + 2087520768),
-    "mxfp4_irregular_8192x65536": ("cd4c5434cfa8448d", 42557696 + 2086157824),
-    "thd_bf16_3seq_8192x32768": ("cd4c5434cfa8448d", 145020928 + 1012817920),
+    "bf16_batched_causal_4096": ("bae21dd70143dde6", 137506048 + 79815936),
+    "fp8_per_token_2048x32768": ("bae21dd70143dde6", 21701376 + 207402752),
+    "mxfp8_2048x32768": ("bae21dd70143dde6", 22223360 + 207762432),
+    "mxfp4_2048x32768": ("bae21dd70143dde6", 11735552 + 207113984),
+    "paged_fp8_decode_64x2_32768": ("bae21dd70143dde6", 208144384 + 8111360),
+    "mxfp8_8192x65536": ("bae21dd70143dde6", 80125184 + 2087665664),
+    "mxfp4_8192x65536": ("bae21dd70143dde6", 42382080 + 2087584256),
+    "mxfp4_irregular_8192x65536": ("bae21dd70143dde6", 42587136 + 2085757184),
+    "thd_bf16_3seq_8192x32768": ("bae21dd70143dde6", 144997632 + 1013131008),
 }
 
 
