@@ -411,17 +411,21 @@ int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
   const int64_t want = (8 * di->sm_count + row_blocks - 1) / row_blocks;
   nchunk = std::max<int64_t>(nchunk, std::min<int64_t>(want, tiles_max));
   nchunk = std::max<int64_t>(nchunk, 1);
-  // Then, among nchunk .. 2*nchunk pieces (at most tiles_max), the count with
-  // the shortest estimated run of the persistent grid: rounds of units
+  // Then, among nchunk/2 .. 2*nchunk pieces (at most tiles_max), the count
+  // with the shortest estimated run of the persistent grid: rounds of units
   // (ceil(units / SMs)) times the tiles of a unit plus about two tiles' worth
   // of per-unit cost (claim, Q block, windows); ties go to fewer units. A
-  // row-block is taken as tiles_max tiles (the host does not read windows).
-  // Measured: 2048 x 32768 calls (2048 units in 13.5 rounds at 4 pieces) take
-  // 5 pieces and run 2% faster; 8192 x 65536 keeps 8.
+  // row-block is taken as tiles_max tiles (the host does not read windows),
+  // so fewer pieces than nchunk are taken only while the grid still runs at
+  // least 16 rounds (unit sizes vary; a short grid's tail does not follow
+  // the estimate). Measured: 2048 x 32768 calls (2048 units in 13.5 rounds
+  // at 4 pieces) take 5 pieces and run 2% faster; 8192 x 65536 calls take 4
+  // instead of 8 (-0.4%).
   {
     int64_t best = nchunk, best_cost = INT64_MAX;
-    for (int64_t n = nchunk; n <= std::min<int64_t>(2 * nchunk, tiles_max); ++n) {
+    for (int64_t n = (nchunk + 1) / 2; n <= std::min<int64_t>(2 * nchunk, tiles_max); ++n) {
       const int64_t rounds = (row_blocks * n + di->sm_count - 1) / di->sm_count;
+      if (n < nchunk && rounds < 16) continue;
       const int64_t cost = rounds * ((tiles_max + n - 1) / n + 2);
       if (cost < best_cost) {
         best = n;
