@@ -130,8 +130,9 @@ typedef struct idx_shape {
  *           negative value is honoured exactly: ReLU(s*x) = |s|*ReLU(-x)).
  *  clean    non-zero: every column j < N outside the window is written -inf.
  *           zero: columns of 128-key tiles that contain no in-window key of
- *           any of the row's 4-row group are left untouched; the rest is
- *           written (-inf outside the window).
+ *           any row of the row's block (4 rows; 2 where every batch has at
+ *           most two rows and the keys are BF16 or E4M3) are left untouched;
+ *           the rest is written (-inf outside the window).
  *  out      FP32 (BF16 with IDX_FLAG_OUT_BF16) [B,S,out_row_stride], base
  *           aligned to its element size; columns >= N are never written.
  *  shape    see idx_shape (host pointer, read during the call only).

@@ -402,9 +402,9 @@ int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
   prm.blocks_per_batch = (sh.S + rb - 1) / rb;
   prm.timeout_ns = static_cast<uint64_t>(g_wait_limit_ns);
 
-  // Units: every row-block split into nchunk pieces of its key tiles. Long
-  // rows get pieces of at most ~64 tiles (load balance across the persistent
-  // grid); small problems get enough pieces for about eight per SM.
+  // Units: every row-block split into nchunk pieces of its key tiles. The
+  // base count gives long rows pieces of at most ~64 tiles and small problems
+  // enough pieces for about eight per SM; the search below then adjusts it.
   const int64_t row_blocks = static_cast<int64_t>(sh.B) * prm.blocks_per_batch;
   const int64_t tiles_max = (sh.N + dsa::kKeysPerTile - 1) / dsa::kKeysPerTile;
   int64_t nchunk = (tiles_max + 63) / 64;
