@@ -142,8 +142,9 @@ typedef struct idx_shape {
  * the host before any launch. A device-side wait that runs out is reported
  * by indexer_get_last_error(), not here. The first call on a (device,
  * stream) pair allocates a small library-owned scratch block (a work counter
- * and an error word, plus B*S words for IDX_FLAG_GROUP_ROWS) from the device's
- * stream-ordered pool; a later call that needs more grows it on `stream`
+ * and an error word, plus B*S words for IDX_FLAG_GROUP_ROWS, plus for the MX
+ * formats 512 bytes per (batch, 128-key tile) holding the key scale words in
+ * the kernel's copy order) from the device's stream-ordered pool; a later call that needs more grows it on `stream`
  * (cudaMallocAsync / cudaFreeAsync, no synchronisation). Make one call of the
  * largest shape before capturing a CUDA graph on that stream, and release a
  * short-lived stream's block with indexer_stream_release;
@@ -350,8 +351,11 @@ IDX_API int indexer_selftest_wait_timeout(int64_t limit_ns, idx_stream_t stream)
  * indexer_selftest_wait_timeout. */
 IDX_API int indexer_noalloc_selftest_wait_timeout(int64_t limit_ns, idx_stream_t stream);
 
-/* Number of kernel launches one indexer_logits call with this shape makes
- * (2 with IDX_FLAG_GROUP_ROWS in effect, else 1); for launch counts in
+/* Number of kernel launches one indexer_logits (or indexer_paged_logits)
+ * call with this shape makes: the logits kernel, plus one with
+ * IDX_FLAG_GROUP_ROWS in effect (the row order) and one for the MX formats
+ * (their key scale words put in the kernel's copy order);
+ * indexer_logits_noalloc makes neither extra launch. For launch counts in
  * benchmarks. */
 IDX_API int indexer_launches_per_call(const idx_shape* shape);
 

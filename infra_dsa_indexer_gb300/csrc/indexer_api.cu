@@ -15,6 +15,7 @@
 #include "dsa_indexer.h"
 #include "indexer_kernel.cuh"
 #include "plan_kernel.cuh"
+#include "scale_order_kernel.cuh"
 #include "topk_kernel.cuh"
 #include "window_kernel.cuh"
 
@@ -29,8 +30,9 @@ struct DeviceInfo {
   int sm_count = 0;
   int cc_major = 0, cc_minor = 0;
   // per kernel instantiation: format, mode, sign, output type, paging (and,
-  // from 128 on, the two-row-block BF16/E4M3 kernels)
-  bool smem_set[136] = {};
+  // from 128 on, the two-row-block BF16/E4M3 kernels, from 136 on the MX
+  // kernels that copy key scales per key)
+  bool smem_set[144] = {};
   bool plan_attr_set = false;
 };
 
@@ -163,13 +165,14 @@ int encode_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, in
 }
 
 template <int FMT, bool NEG_EPI, bool OUT_BF16, bool PAGED, int MODE = dsa::kModeLogits,
-          int RB = dsa::kRowsPerBlock>
+          int RB = dsa::kRowsPerBlock, bool SF_KEYS = false>
 int launch_kernel(const KernelParams& prm, int grid, DeviceInfo* di, cudaStream_t stream) {
   constexpr int smem = dsa::Layout<FMT, RB>::kBytes;
-  auto kern = dsa::indexer_logits_kernel<FMT, NEG_EPI, OUT_BF16, PAGED, MODE, RB>;
+  auto kern = dsa::indexer_logits_kernel<FMT, NEG_EPI, OUT_BF16, PAGED, MODE, RB, SF_KEYS>;
   static_assert(RB == dsa::kRowsPerBlock || FMT < 2, "two-row blocks: BF16 and E4M3");
   bool& attr_set =
-      di->smem_set[RB == dsa::kRowsPerBlock
+      di->smem_set[SF_KEYS ? 136 + (FMT - 2) * 4 + (NEG_EPI ? 2 : 0) + (OUT_BF16 ? 1 : 0)
+                   : RB == dsa::kRowsPerBlock
                        ? FMT * 32 + MODE * 8 + (NEG_EPI ? 4 : 0) + (OUT_BF16 ? 2 : 0) +
                              (PAGED ? 1 : 0)
                        : 128 + FMT * 4 + (OUT_BF16 ? 2 : 0) + (PAGED ? 1 : 0)];
@@ -205,6 +208,16 @@ int launch(const KernelParams& prm, int grid, DeviceInfo* di, cudaStream_t strea
                           : launch_kernel<FMT, false, false, false, kM, 2>(prm, grid, di, stream);
     }
   }
+  if constexpr (FMT == dsa::kFmtMXFP8 || FMT == dsa::kFmtMXFP4) {
+    // No key scales in copy order (no library scratch): per-key copies.
+    if (prm.k_sf_tiles == nullptr) {
+      if (mode != dsa::kModeLogits || prm.block_table != nullptr) return IDX_ERR_UNSUPPORTED;
+      constexpr int kM = dsa::kModeLogits, kR = dsa::kRowsPerBlock;
+      return prm.out_bf16
+                 ? launch_kernel<FMT, NEG_EPI, true, false, kM, kR, true>(prm, grid, di, stream)
+                 : launch_kernel<FMT, NEG_EPI, false, false, kM, kR, true>(prm, grid, di, stream);
+    }
+  }
   if (mode == dsa::kModeSample)
     return launch_kernel<FMT, NEG_EPI, false, false, dsa::kModeSample>(prm, grid, di, stream);
   if (mode == dsa::kModeFilter)
@@ -223,7 +236,9 @@ extern "C" {
 int indexer_version(void) { return 200; }
 
 int indexer_launches_per_call(const idx_shape* shape) {
-  return shape != nullptr && groups_rows(*shape, false) ? 2 : 1;
+  if (shape == nullptr) return 1;
+  const bool mx = shape->fmt == IDX_FMT_MXFP8 || shape->fmt == IDX_FMT_MXFP4;
+  return 1 + (groups_rows(*shape, false) ? 1 : 0) + (mx ? 1 : 0);
 }
 
 const char* indexer_status_string(int status) {
@@ -333,14 +348,20 @@ int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
   if (di->cc_major != 10 || di->cc_minor != 3) return IDX_ERR_DEVICE;
   if ((st = get_encoder())) return st;
   int32_t* scratch = nullptr;
+  // MX key scale words in copy order (scale_order_kernel), 128 words per
+  // (batch, key tile), after the header words and the row order; not with
+  // the fixed array (the kernel then copies them per key).
+  const bool sf_order = (sh.fmt == IDX_FMT_MXFP8 || sh.fmt == IDX_FMT_MXFP4) && !fixed_scratch;
+  const int64_t key_tiles = (static_cast<int64_t>(sh.N) + dsa::kKeysPerTile - 1) / dsa::kKeysPerTile;
+  const int64_t sf_off =
+      (kScratchInts + (groups_rows(sh, fixed_scratch) ? total_rows : 0) + 63) / 64 * 64;
+  const int64_t sf_words = sf_order ? static_cast<int64_t>(sh.B) * key_tiles * 128 : 0;
   if (fixed_scratch) {
     if ((st = get_fixed_scratch(dev, &scratch))) return st;
     // The array keeps the previous call's words: start this one from zero.
     if (cudaMemsetAsync(scratch, 0, kScratchWordsPerCall * sizeof(int32_t), stream) != cudaSuccess)
       return IDX_ERR_CUDA;
-  } else if ((st = get_scratch(dev, stream,
-                                kScratchInts + (groups_rows(sh, fixed_scratch) ? total_rows : 0),
-                                &scratch))) {
+  } else if ((st = get_scratch(dev, stream, sf_order ? sf_off + sf_words : sf_off, &scratch))) {
     return st;
   }
 
@@ -444,6 +465,21 @@ int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
     if (!pass.planned &&
         (st = launch_plan(ks, ke, sh, const_cast<int32_t*>(prm.perm), di, stream)))
       return st;
+  }
+  if (sf_order) {
+    uint32_t* sf = reinterpret_cast<uint32_t*>(scratch + sf_off);
+    prm.k_sf_tiles = reinterpret_cast<const uint8_t*>(sf);
+    // The fused call's second pass reuses the first pass's words.
+    if (!pass.planned) {
+      const int threads = 256;
+      const int64_t blocks = std::min<int64_t>((sf_words + threads - 1) / threads,
+                                               static_cast<int64_t>(di->sm_count) * 8);
+      dsa::scale_order_kernel<<<static_cast<int>(blocks), threads, 0, stream>>>(
+          reinterpret_cast<const uint32_t*>(k_sf), sh.N, static_cast<int>(key_tiles), sf_words,
+          paged ? pg.block_table : nullptr, paged ? pg.table_stride : 0,
+          paged ? pg.page_size : 0, paged ? pg.num_pages : 0, sf);
+      if (cudaGetLastError() != cudaSuccess) return IDX_ERR_CUDA;
+    }
   }
 
   const int mode = pass.mode;

@@ -136,6 +136,9 @@ struct KernelParams {
   CUtensorMap tmap_k;  // [B, N, D] view of K, or [pages * page_size, D] of a paged cache
   const uint8_t* q_sf;
   const uint8_t* k_sf;
+  // MX formats: the key scale words in tensor-memory copy order, 512 bytes per
+  // (batch, 128-key tile) (scale_order_kernel); unused with SF_KEYS.
+  const uint8_t* k_sf_tiles;
   const float* k_scales;
   const void* w;
   const int32_t* ks;
@@ -277,17 +280,6 @@ __device__ __forceinline__ int clampi(int v, int lo, int hi) {
   return v < lo ? lo : (v > hi ? hi : v);
 }
 
-// Cache row of key j (0 <= j < N) of batch b: j itself past the batch's
-// first key for contiguous keys, else through the page table.
-template <bool PAGED>
-__device__ __forceinline__ int64_t key_row(const KernelParams& p, int b, int j) {
-  if constexpr (!PAGED) return static_cast<int64_t>(b) * p.N + j;
-  const int page = clampi(
-      __ldg(p.block_table + static_cast<int64_t>(b) * p.table_stride + j / p.page_size), 0,
-      p.num_pages - 1);
-  return static_cast<int64_t>(page) * p.page_size + j % p.page_size;
-}
-
 __device__ __forceinline__ void raise_error(int32_t* scratch, volatile int* abort_flag, int code) {
   *abort_flag = 1;
   atomicExch(scratch + 2, code);
@@ -382,12 +374,20 @@ __device__ __forceinline__ void mma_step(uint32_t d_tmem, uint64_t a_desc, uint6
 // PAGED: the keys (and key scales) are read through the page table.
 // MODE: kModeLogits, or one of the two passes of the fused top-k call.
 // RB: rows per block (Layout).
+// SF_KEYS (MX formats): the K producer copies each key's scale word itself
+// (128 four-byte copies per tile, counted on their own barrier) instead of
+// one bulk copy of the tile's words put in order beforehand; for calls
+// without library scratch. A compile-time choice: as a run-time flag in the
+// producer and MMA issuer loops it cost the MXFP8 kernel the whole 4% the
+// bulk copy gains.
 template <int FMT, bool NEG_EPI, bool OUT_BF16, bool PAGED, int MODE = kModeLogits,
-          int RB = kRowsPerBlock>
+          int RB = kRowsPerBlock, bool SF_KEYS = false>
 __global__ void __launch_bounds__(Layout<FMT, RB>::kThreads, 1)
     indexer_logits_kernel(const __grid_constant__ KernelParams p) {
   static_assert(MODE == kModeLogits || (!OUT_BF16 && !PAGED), "fused top-k: FP32, contiguous keys");
   static_assert(RB == kRowsPerBlock || MODE == kModeLogits, "fused top-k: four-row blocks");
+  static_assert(!SF_KEYS || (Traits<FMT>::kMX && !PAGED && MODE == kModeLogits),
+                "per-key scale copies: contiguous MX logits only");
   using T = Traits<FMT>;
   using L = Layout<FMT, RB>;
   constexpr int kNumEpiWarps = L::kNumEpiWarps;
@@ -672,6 +672,10 @@ __global__ void __launch_bounds__(Layout<FMT, RB>::kThreads, 1)
     // word c of the 16-byte rows the TMEM copy reads); for paged keys all
     // lanes hold block-table entries (page_entry).
     constexpr bool kWarpWide = T::kMX || PAGED;
+    // MX: a tile's key scale words come in one bulk copy on the tile's own
+    // barrier (put in copy order beforehand), or per key with SF_KEYS.
+    constexpr bool sf_bulk = T::kMX && !SF_KEYS;
+    const int sf_tiles = (p.N + kKeysPerTile - 1) / kKeysPerTile;
     if (lane == 0) prefetch_tmap(&p.tmap_k);
     // K is re-read by every row-block of its batch: kept in L2 (evict_last),
     // except where a batch has at most two row-blocks (decode), whose keys are
@@ -742,7 +746,11 @@ __global__ void __launch_bounds__(Layout<FMT, RB>::kThreads, 1)
         if constexpr (kWarpWide) ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&k_full[st], L::kKTileBytes);
+          mbar_arrive_expect_tx(&k_full[st], L::kKTileBytes + (sf_bulk ? kSfaBytes : 0));
+          if constexpr (sf_bulk)
+            bulk_load(sfa_s + st * kSfaBytes,
+                      p.k_sf_tiles + (static_cast<int64_t>(b) * sf_tiles + t) * kSfaBytes,
+                      kSfaBytes, &k_full[st]);
           uint8_t* kdst = kbuf + st * L::kKTileBytes;
           if constexpr (!PAGED) {
 #pragma unroll
@@ -759,22 +767,13 @@ __global__ void __launch_bounds__(Layout<FMT, RB>::kThreads, 1)
                             pol_k);
           }
         }
-        if constexpr (T::kMX) {
+        if constexpr (T::kMX && SF_KEYS) {
           uint8_t* dst = sfa_s + st * kSfaBytes + 16 * lane;
-          if constexpr (!PAGED) {
-            const uint8_t* src =
-                p.k_sf + (static_cast<int64_t>(b) * p.N + t * kKeysPerTile) * 4;
+          const uint8_t* src = p.k_sf + (static_cast<int64_t>(b) * p.N + t * kKeysPerTile) * 4;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int m = 32 * c + lane;
-              if (t * kKeysPerTile + m < p.N) cp_async_4(dst + 4 * c, src + 4 * m);
-            }
-          } else {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int j = t * kKeysPerTile + 32 * c + lane;
-              if (j < p.N) cp_async_4(dst + 4 * c, p.k_sf + key_row<PAGED>(p, b, j) * 4);
-            }
+          for (int c = 0; c < 4; ++c) {
+            const int m = 32 * c + lane;
+            if (t * kKeysPerTile + m < p.N) cp_async_4(dst + 4 * c, src + 4 * m);
           }
           cp_async_arrive(&sf_full[st]);
         }
@@ -789,7 +788,7 @@ __global__ void __launch_bounds__(Layout<FMT, RB>::kThreads, 1)
       // before the CTA exits.
       for (uint32_t j = kiter > T::kStages ? kiter - T::kStages : 0; j < kiter; ++j) {
         mbar_wait_drain(&k_full[j % T::kStages], (j / T::kStages) & 1, p.timeout_ns);
-        if constexpr (T::kMX)
+        if constexpr (T::kMX && SF_KEYS)
           mbar_wait_drain(&sf_full[j % T::kStages], (j / T::kStages) & 1, p.timeout_ns);
       }
     }
@@ -825,7 +824,7 @@ __global__ void __launch_bounds__(Layout<FMT, RB>::kThreads, 1)
         const uint32_t kpar = (kiter / T::kStages) & 1;
         const uint32_t apar = ((aiter / kAccBufs) & 1) ^ 1;
         if (!mbar_wait(&k_full[st], kpar, abort_flag, p.timeout_ns) ||
-            (T::kMX && !mbar_wait(&sf_full[st], kpar, abort_flag, p.timeout_ns))) {
+            (T::kMX && SF_KEYS && !mbar_wait(&sf_full[st], kpar, abort_flag, p.timeout_ns))) {
           ok = false;
           break;
         }

@@ -49,6 +49,8 @@ def test_status_strings(lib):
     assert binding.indexer_launches_per_call(shp()) == 1
     assert binding.indexer_launches_per_call(shp(flags=1)) == 2
     assert binding.indexer_launches_per_call(shp(flags=1, S=16388)) == 2   # any S
+    assert binding.indexer_launches_per_call(shp(fmt=2)) == 2              # MX: scale order
+    assert binding.indexer_launches_per_call(shp(fmt=3, flags=1)) == 3
 
 
 FAKE = ctypes.c_void_p(0x1000)      # never dereferenced: validation fails first
