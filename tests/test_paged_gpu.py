@@ -50,3 +50,27 @@ def test_paged_decode_windows(fmt, S):
     assert torch.equal(op.view(torch.int32), oc.view(torch.int32))
     ref, den = oracle_rows(case)
     compare(op.view(-1, case.N).cpu().numpy(), ref, den)
+
+
+@pytest.mark.parametrize("out_bf16", [False, True])
+@pytest.mark.parametrize("S", [3, 5, 6, 7])
+def test_paged_e4m3_partial_blocks(S, out_bf16):
+    """Paged E4M3 four-row blocks (two epilogue groups on alternate tiles,
+    each warp reducing two rows in turn) with a partial last block, several
+    chunks per block and FP32 or BF16 logits: bit-equal to the contiguous
+    call, and within the bound of the oracle."""
+    import dataclasses
+    case = synth.make_case(synth.FMT_E4M3, 2, S, 2600, seed=160 + S, windows="irregular",
+                           page_size=64)
+    flat = dataclasses.replace(case, page_size=0)
+    tp = binding.case_to_device(case, out_bf16=out_bf16)
+    tc = binding.case_to_device(flat, out_bf16=out_bf16)
+    binding.run_case(case, tp)
+    binding.run_case(flat, tc)
+    torch.cuda.synchronize()
+    assert binding.indexer_get_last_error() == binding.IDX_OK
+    assert torch.equal(tp["out"].view(torch.int16 if out_bf16 else torch.int32),
+                       tc["out"].view(torch.int16 if out_bf16 else torch.int32))
+    ref, den = oracle_rows(case)
+    compare(tp["out"].float().view(-1, case.N).cpu().numpy(), ref, den,
+            out_rounding=2.0 ** -8 if out_bf16 else 0.0)
