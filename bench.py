@@ -64,15 +64,15 @@ KERNEL_FILES = ("indexer_kernel.cuh", "ptx.cuh", "plan_kernel.cuh")
 # DRAM bytes (read + write) of one logits-kernel launch from an ncu capture,
 # keyed by workload, with the kernel-source digest it was taken on.
 PROFILED_TRAFFIC = {
-    "bf16_batched_causal_4096": ("bae21dd70143dde6", 137506048 + 79815936),
-    "fp8_per_token_2048x32768": ("bae21dd70143dde6", 21701376 + 207402752),
-    "mxfp8_2048x32768": ("bae21dd70143dde6", 22223360 + 207762432),
-    "mxfp4_2048x32768": ("bae21dd70143dde6", 11735552 + 207113984),
-    "paged_fp8_decode_64x2_32768": ("bae21dd70143dde6", 208144384 + 8111360),
-    "mxfp8_8192x65536": ("bae21dd70143dde6", 80125184 + 2087665664),
-    "mxfp4_8192x65536": ("bae21dd70143dde6", 42382080 + 2087584256),
-    "mxfp4_irregular_8192x65536": ("bae21dd70143dde6", 42587136 + 2085757184),
-    "thd_bf16_3seq_8192x32768": ("bae21dd70143dde6", 144997632 + 1013131008),
+    "bf16_batched_causal_4096": ("f24bafa159091945", 137480192 + 79400448),
+    "fp8_per_token_2048x32768": ("f24bafa159091945", 21690368 + 207807232),
+    "mxfp8_2048x32768": ("f24bafa159091945", 22222080 + 207803392),
+    "mxfp4_2048x32768": ("f24bafa159091945", 11733248 + 207256320),
+    "paged_fp8_decode_64x2_32768": ("f24bafa159091945", 208142336 + 7953152),
+    "mxfp8_8192x65536": ("f24bafa159091945", 81149440 + 2087088128),
+    "mxfp4_8192x65536": ("f24bafa159091945", 42714368 + 2086714880),
+    "mxfp4_irregular_8192x65536": ("f24bafa159091945", 43566848 + 2086211328),
+    "thd_bf16_3seq_8192x32768": ("f24bafa159091945", 144908800 + 1012556032),
 }
 
 
