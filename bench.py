@@ -60,7 +60,7 @@ L2_FLUSH_BYTES = 256 << 20
 # Files that define the logits kernel: a DRAM-traffic figure taken with ncu
 # (profiles/) is reported as roofline.traffic only while these still hash to
 # the digest it was taken on.
-KERNEL_FILES = ("indexer_kernel.cuh", "ptx.cuh", "plan_kernel.cuh")
+KERNEL_FILES = ("indexer_kernel.cuh", "ptx.cuh", "plan_kernel.cuh", "page_div.h")
 # DRAM bytes (read + write) of one logits-kernel launch from an ncu capture,
 # keyed by workload, with the kernel-source digest it was taken on.
 PROFILED_TRAFFIC = {

@@ -396,6 +396,9 @@ int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
       if ((st = encode_map(&prm.tmap_k, k, dt, 2, dims, strides, box, swz))) return st;
       prm.block_table = pg.block_table;
       prm.page_size = pg.page_size;
+      const dsa::PageDiv pdiv = dsa::page_div_make(static_cast<uint32_t>(pg.page_size));
+      prm.page_magic = pdiv.magic;
+      prm.page_shift = pdiv.shift;
       prm.table_stride = pg.table_stride;
       prm.num_pages = pg.num_pages;
     }

@@ -28,19 +28,24 @@
 //    windows the highest row index), so the persistent grid balances itself.
 //
 // Roles (one CTA per SM; 4 role warps + 8 or 16 epilogue warps):
-//  warp 0       K-tile TMA producer (lane 0; paged keys: two 64-key boxes per
-//               tile, each inside one page); for MX formats the tile's key
-//               scale factors come along, one 512-byte bulk copy of words a
-//               pre-pass put in the order the TMEM copy reads (without
-//               library scratch, all 32 lanes copy them key by key)
+//  warp 0       K-tile TMA producer (lane 0; paged keys: the first of the
+//               tile's two 64-key boxes, each inside one page); for MX
+//               formats the tile's key scale factors come along, one 512-byte
+//               bulk copy of words a pre-pass put in the order the TMEM copy
+//               reads (without library scratch, all 32 lanes copy them key by
+//               key)
 //  warp 1       TMEM allocator + MMA issuer (one lane)
 //  warp 2       unit scheduler: claims a unit and fetches its windows, head
 //               weights and (MX) Q scale factors into registers; when the Q
 //               half of a slot frees it starts the TMA of the unit's Q block
 //               (and stages the Q scale factors), when the epilogue half
 //               frees it stages the weights in shared memory as FP32 and the
-//               windows, one unit ahead of the MMA
-//  warp 3       idle
+//               windows, one unit ahead of the MMA; with paged keys it also
+//               copies the unit's first 32 block-table entries for the
+//               producers and the epilogue
+//  warp 3       paged keys: the second 64-key box of every tile (one thread
+//               issuing TMA boxes of 8 KB tops out near 4.4 TB/s of HBM per
+//               GPU; two issuing warps near 6.9), else idle
 //  warps 4..    epilogue, R = 1 or 2 query rows per warp (a per-format
 //               choice): warp w reads TMEM lanes 32*(w%4)..+31 (the
 //               sub-partition it may access) of rows R*((w-4)/4) .. +R-1; it
@@ -63,6 +68,7 @@
 #include <cuda.h>
 #include <cstdint>
 
+#include "page_div.h"
 #include "ptx.cuh"
 
 namespace dsa {
@@ -153,6 +159,8 @@ struct KernelParams {
   // the cache; key scales (k_sf, k_scales) follow the same rows.
   const int32_t* block_table;
   int32_t page_size;     // multiple of 64
+  uint32_t page_magic;   // page_div_make(page_size): key / page_size without a division
+  int32_t page_shift;
   int32_t table_stride;
   int32_t num_pages;     // page numbers are clamped to [0, num_pages)
   void* out;         // FP32, or BF16 when out_bf16; the compact sample rows
@@ -271,7 +279,8 @@ struct Layout {
   static constexpr int kSfbOff = kSfaOff + (T::kMX ? T::kStages * kSfaBytes : 0);
   static constexpr int kInfoOff = kSfbOff + (T::kMX ? 2 * kSfbBytes : 0);
   static constexpr int kQInfoOff = kInfoOff + 2 * (int)sizeof(UnitInfo);
-  static constexpr int kBarOff = kQInfoOff + 2 * (int)sizeof(QInfo);
+  static constexpr int kPagesOff = kQInfoOff + 2 * (int)sizeof(QInfo);
+  static constexpr int kBarOff = kPagesOff + 4 * 32 * 4;  // paged: 32 table entries x 4
   static constexpr int kNumBars =
       2 + 2 + 2 * T::kStages + 2 * kAccBufs + (T::kMX ? T::kStages : 0) + 1 + 2 + 2;
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
@@ -281,6 +290,11 @@ struct Layout {
 
 __device__ __forceinline__ int clampi(int v, int lo, int hi) {
   return v < lo ? lo : (v > hi ? hi : v);
+}
+
+// Page of key (or cache row) j of a paged cache: j / page_size (j >= 0).
+__device__ __forceinline__ int page_index(const KernelParams& p, int j) {
+  return static_cast<int>(page_div(static_cast<uint32_t>(j), p.page_magic, p.page_shift));
 }
 
 __device__ __forceinline__ void raise_error(int32_t* scratch, volatile int* abort_flag, int code) {
@@ -415,6 +429,9 @@ __global__ void __launch_bounds__(Layout<FMT, RB>::kThreads, 1)
   uint8_t* sfb_s = smem + L::kSfbOff;  // [2 slots][256 rows x 4 bytes], TMEM-copy order
   UnitInfo* info = reinterpret_cast<UnitInfo*>(smem + L::kInfoOff);
   QInfo* qinfo = reinterpret_cast<QInfo*>(smem + L::kQInfoOff);
+  // Paged keys: the first 32 block-table entries of each slot's unit, copied
+  // by the scheduler for the K producer ([slot]) and the epilogue ([2 + slot]).
+  int32_t* unit_pages = reinterpret_cast<int32_t*>(smem + L::kPagesOff);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   // A unit slot has two halves: the Q half (Q block, MX Q scales, QInfo;
   // q_full / q_empty), read by the K producer and the MMA issuer and
@@ -455,7 +472,7 @@ __global__ void __launch_bounds__(Layout<FMT, RB>::kThreads, 1)
       mbar_init(&acc_empty[s], kGroupWarps);  // the warps of the group that drains it
     }
     for (int s = 0; s < T::kStages; ++s) {
-      mbar_init(&k_full[s], 1);
+      mbar_init(&k_full[s], PAGED ? 2 : 1);  // paged: one arrive per producer warp
       mbar_init(&k_empty[s], 1);
       if constexpr (T::kMX) mbar_init(&sf_full[s], 32);
     }
@@ -494,6 +511,7 @@ __global__ void __launch_bounds__(Layout<FMT, RB>::kThreads, 1)
       int grow[kRowsPerBlock];
       UnitInfo in;      // lane 0 only: the info the slot gets
       float4 w[2];      // this lane's part of the block's FP32 head weights
+      int32_t pg;       // paged keys: table entry `lane` of the unit's first page on
       uint32_t sf[kBlockN / 32];  // MX: this lane's Q scale words
     };
     // grow[i] for a lane-dependent i, without indexing the array at run time
@@ -549,6 +567,18 @@ __global__ void __launch_bounds__(Layout<FMT, RB>::kThreads, 1)
         q.in.t0 = t0;
         q.in.t1 = t1;
         q.in.flags = (q.chunk == 0 ? 1 : 0) | (q.chunk == p.nchunk - 1 ? 2 : 0);
+      }
+      if constexpr (PAGED) {
+        // The unit's first 32 table entries, loaded with the weights: the K
+        // producer and the epilogue start the unit without waiting for the
+        // table.
+        const int c0 = __shfl_sync(0xffffffffu, q.in.c0, 0);
+        const int c1 = __shfl_sync(0xffffffffu, q.in.c1, 0);
+        const int e = page_index(p, c0 * kKeysPerTile) + lane;
+        const int n_e = page_index(p, p.N - 1) + 1;
+        q.pg = c0 < c1 && e < n_e
+                   ? __ldg(p.block_table + static_cast<int64_t>(q.b) * p.table_stride + e)
+                   : 0;
       }
       if (p.w_bf16) {
         // lane l: 8 weights = 16 bytes, row l/8, heads 8*(l%8).. (rows past
@@ -658,11 +688,13 @@ __global__ void __launch_bounds__(Layout<FMT, RB>::kThreads, 1)
           *reinterpret_cast<uint32_t*>(dst + (m >> 7) * 512 + 16 * lane + 4 * (c & 3)) = cur.sf[c];
         }
       }
+      if constexpr (PAGED) unit_pages[slot * 32 + lane] = cur.pg;
       __syncwarp();
       if (lane == 0) mbar_arrive(&q_full[slot]);
       // Epilogue half: free once the epilogue is done with unit it-2.
       if (!wait_half(unit_empty, it, it > 1 ? it - 1 : 0, it + 1)) break;
       if (lane == 0) in = cur.in;
+      if constexpr (PAGED) unit_pages[(2 + slot) * 32 + lane] = cur.pg;
       // Head weights of the RB rows as FP32, row-major RB x 64.
       float4* wdst = reinterpret_cast<float4*>(wbuf + slot * L::kWBytes);
       if (p.w_bf16) {
@@ -678,12 +710,18 @@ __global__ void __launch_bounds__(Layout<FMT, RB>::kThreads, 1)
       if (lane == 0) mbar_arrive(&unit_full[slot]);
       if (ahead) prepare(__shfl_sync(0xffffffffu, u_next, 0), cur);
     }
-  } else if (warp == 0 && (T::kMX || PAGED || lane == 0)) {
+  } else if (PAGED ? (warp == 0 || warp == 3) : (warp == 0 && (T::kMX || lane == 0))) {
+    // (Written as a compile-time choice: the form "warp 0 or, with paged
+    // keys, warp 3" in one expression cost the contiguous E4M3 kernel 2.4%.)
     // ------------------------------------------------------- K-tile producer
     // Lane 0 waits and issues the TMA; for MX formats all lanes also copy the
     // tile's 128 key scale words (word of key m = 32c + lane to row `lane`,
     // word c of the 16-byte rows the TMEM copy reads); for paged keys all
-    // lanes hold block-table entries (page_entry).
+    // lanes hold block-table entries (page_entry), and warps 0 and 3 each
+    // issue one of the tile's two 64-key boxes (box `half`), each with its
+    // own arrival and byte count on the stage's barrier: one thread issuing
+    // 8 KB boxes cannot keep enough of them in flight to stream HBM.
+    const int half = PAGED && warp == 3 ? 1 : 0;
     constexpr bool kWarpWide = T::kMX || PAGED;
     // MX: a tile's key scale words come in one bulk copy on the tile's own
     // barrier (put in copy order beforehand), or per key with SF_KEYS.
@@ -699,7 +737,7 @@ __global__ void __launch_bounds__(Layout<FMT, RB>::kThreads, 1)
     // entry `win` + l (`cur`) and `win` + 32 + l (`nxt`). The next 32 are
     // requested on entering a window, so the table's latency is spread over
     // the tiles of 32 entries instead of stalling every TMA issue.
-    const int n_entries = PAGED ? (p.N + p.page_size - 1) / p.page_size : 0;
+    const int n_entries = PAGED ? page_index(p, p.N - 1) + 1 : 0;
     const int32_t* table = nullptr;
     int win = 0, cur = 0, nxt = 0;
     auto fetch_entry = [&](int e) { return e < n_entries ? __ldg(table + e) : 0; };
@@ -736,8 +774,8 @@ __global__ void __launch_bounds__(Layout<FMT, RB>::kThreads, 1)
       const int c0 = qi.c0, c1 = qi.c1, b = qi.b;
       if constexpr (PAGED) {
         table = p.block_table + static_cast<int64_t>(b) * p.table_stride;
-        win = c0 * kKeysPerTile / p.page_size;
-        cur = fetch_entry(win + lane);
+        win = page_index(p, c0 * kKeysPerTile);
+        cur = unit_pages[slot * 32 + lane];  // the scheduler's copy of entry win + lane
         nxt = fetch_entry(win + 32 + lane);
       }
       for (int t = first_tile<MODE>(c0); t < c1; t = next_tile<MODE>(t), ++kiter) {
@@ -750,8 +788,8 @@ __global__ void __launch_bounds__(Layout<FMT, RB>::kThreads, 1)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int k0 = t * kKeysPerTile + 64 * h;
-            prow[h] = k0 < p.N ? page_entry(k0 / p.page_size) * p.page_size + k0 % p.page_size
-                               : prow[0];
+            const int e = page_index(p, k0);
+            prow[h] = k0 < p.N ? page_entry(e) * p.page_size + (k0 - e * p.page_size) : prow[0];
           }
         }
         if (lane == 0)
@@ -759,11 +797,13 @@ __global__ void __launch_bounds__(Layout<FMT, RB>::kThreads, 1)
         if constexpr (kWarpWide) ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&k_full[st], L::kKTileBytes + (sf_bulk ? kSfaBytes : 0));
+          mbar_arrive_expect_tx(&k_full[st], (PAGED ? L::kKTileBytes / 2 : L::kKTileBytes) +
+                                                 (sf_bulk && half == 0 ? kSfaBytes : 0));
           if constexpr (sf_bulk)
-            bulk_load(sfa_s + st * kSfaBytes,
-                      p.k_sf_tiles + (static_cast<int64_t>(b) * sf_tiles + t) * kSfaBytes,
-                      kSfaBytes, &k_full[st]);
+            if (half == 0)
+              bulk_load(sfa_s + st * kSfaBytes,
+                        p.k_sf_tiles + (static_cast<int64_t>(b) * sf_tiles + t) * kSfaBytes,
+                        kSfaBytes, &k_full[st]);
           uint8_t* kdst = kbuf + st * L::kKTileBytes;
           if constexpr (!PAGED) {
 #pragma unroll
@@ -772,12 +812,10 @@ __global__ void __launch_bounds__(Layout<FMT, RB>::kThreads, 1)
                           pnl * (T::kSwizzleBytes / T::kTmaElemBytes), t * kKeysPerTile, b, pol_k);
           } else {
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-              for (int pnl = 0; pnl < L::kPanels; ++pnl)
-                tma_load_2d(kdst + pnl * L::kKPanelBytes + h * 64 * T::kSwizzleBytes, &p.tmap_k,
-                            &k_full[st], pnl * (T::kSwizzleBytes / T::kTmaElemBytes), prow[h],
-                            pol_k);
+            for (int pnl = 0; pnl < L::kPanels; ++pnl)
+              tma_load_2d(kdst + pnl * L::kKPanelBytes + half * 64 * T::kSwizzleBytes, &p.tmap_k,
+                          &k_full[st], pnl * (T::kSwizzleBytes / T::kTmaElemBytes),
+                          half ? prow[1] : prow[0], pol_k);
           }
         }
         if constexpr (T::kMX && SF_KEYS) {
@@ -982,20 +1020,29 @@ __global__ void __launch_bounds__(Layout<FMT, RB>::kThreads, 1)
         const int jj = t * kKeysPerTile + quarter * 32 + lane;
         if (!(key_scaled && t < c1 && jj < p.N)) return -1;
         return clampi(__ldg(p.block_table + static_cast<int64_t>(b) * p.table_stride +
-                            jj / p.page_size),
+                            page_index(p, jj)),
                       0, p.num_pages - 1);
       };
       auto scale_in_page = [&](int t, int page) {
         if (page < 0) return 1.f;
         const int jj = t * kKeysPerTile + quarter * 32 + lane;
-        return __ldg(p.k_scales + static_cast<int64_t>(page) * p.page_size + jj % p.page_size);
+        return __ldg(p.k_scales + static_cast<int64_t>(page) * p.page_size +
+                     (jj - page_index(p, jj) * p.page_size));
       };
       // This group's first tile of the unit; its later ones are kGroups
       // apart (kGroups > 1 only computes logits, where tiles are consecutive).
       const int tf = first_tile<MODE>(c0) +
                      (kGroups > 1 ? static_cast<int>((grp + kGroups - aiter % kGroups) % kGroups) : 0);
-      int page_ahead = PAGED ? load_page(tf + kGroups) : -1;
-      float kscale_next = PAGED ? scale_in_page(tf, load_page(tf)) : load_kscale(tf);
+      // The unit's first pages come from the scheduler's copy of its first
+      // 32 table entries: no wait for the table at the unit's start.
+      auto first_page = [&](int t) {
+        const int jj = t * kKeysPerTile + quarter * 32 + lane;
+        if (!(key_scaled && t < c1 && jj < p.N)) return -1;
+        const int e = page_index(p, jj) - page_index(p, c0 * kKeysPerTile);
+        return e < 32 ? clampi(unit_pages[(2 + slot) * 32 + e], 0, p.num_pages - 1) : load_page(t);
+      };
+      int page_ahead = PAGED ? first_page(tf + kGroups) : -1;
+      float kscale_next = PAGED ? scale_in_page(tf, first_page(tf)) : load_kscale(tf);
       bool ok = true;
       if (PAGED && !any_row) {
         // Every row of this warp is past S (a partial last block; decode with

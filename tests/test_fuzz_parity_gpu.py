@@ -43,7 +43,7 @@ def draw(seed):
     kw = dict(seed=9100 + seed,
               w_fmt=synth.W_BF16 if rng.random() < 0.3 else synth.W_F32,
               sm_scale=float((-1.0 if rng.random() < 0.3 else 1.0) * rng.uniform(0.02, 0.2)),
-              page_size=int(rng.choice([0, 0, 64, 128, 256])))
+              page_size=int(rng.choice([0, 0, 64, 128, 192, 256])))
     if kind == "random":
         ks = rng.integers(-50, N + 50, size=(B, S))
         ke = ks + rng.integers(-100, N + 100, size=(B, S))
