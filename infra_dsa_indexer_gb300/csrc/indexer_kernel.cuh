@@ -780,17 +780,16 @@ __global__ void __launch_bounds__(Layout<FMT, RB>::kThreads, 1)
       }
       for (int t = first_tile<MODE>(c0); t < c1; t = next_tile<MODE>(t), ++kiter) {
         const int st = kiter % T::kStages;
-        // Rows of the tile's two 64-key boxes, each inside one page (page_size
-        // is a multiple of 64). The first box starts below N; a second box
-        // wholly past N re-reads the first one's rows (keys no window reads).
+        // Rows of this warp's 64-key box (keys 64*half.. of the tile), inside
+        // one page (page_size is a multiple of 64). The first box starts
+        // below N; a second box wholly past N re-reads the first one's rows
+        // (keys no window reads).
         int prow[2] = {0, 0};
         if constexpr (PAGED) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int k0 = t * kKeysPerTile + 64 * h;
-            const int e = page_index(p, k0);
-            prow[h] = k0 < p.N ? page_entry(e) * p.page_size + (k0 - e * p.page_size) : prow[0];
-          }
+          const int k0 = t * kKeysPerTile + 64 * half;
+          const int kk = k0 < p.N ? k0 : k0 - 64;
+          const int e = page_index(p, kk);
+          prow[0] = page_entry(e) * p.page_size + (kk - e * p.page_size);
         }
         if (lane == 0)
           ok = mbar_wait(&k_empty[st], ((kiter / T::kStages) & 1) ^ 1, abort_flag, p.timeout_ns);
@@ -814,8 +813,8 @@ __global__ void __launch_bounds__(Layout<FMT, RB>::kThreads, 1)
 #pragma unroll
             for (int pnl = 0; pnl < L::kPanels; ++pnl)
               tma_load_2d(kdst + pnl * L::kKPanelBytes + half * 64 * T::kSwizzleBytes, &p.tmap_k,
-                          &k_full[st], pnl * (T::kSwizzleBytes / T::kTmaElemBytes),
-                          half ? prow[1] : prow[0], pol_k);
+                          &k_full[st], pnl * (T::kSwizzleBytes / T::kTmaElemBytes), prow[0],
+                          pol_k);
           }
         }
         if constexpr (T::kMX && SF_KEYS) {
