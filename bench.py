@@ -64,15 +64,15 @@ KERNEL_FILES = ("indexer_kernel.cuh", "ptx.cuh", "plan_kernel.cuh", "page_div.h"
 # DRAM bytes (read + write) of one logits-kernel launch from an ncu capture,
 # keyed by workload, with the kernel-source digest it was taken on.
 PROFILED_TRAFFIC = {
-    "bf16_batched_causal_4096": ("f24bafa159091945", 137480192 + 79400448),
-    "fp8_per_token_2048x32768": ("f24bafa159091945", 21690368 + 207807232),
-    "mxfp8_2048x32768": ("f24bafa159091945", 22222080 + 207803392),
-    "mxfp4_2048x32768": ("f24bafa159091945", 11733248 + 207256320),
-    "paged_fp8_decode_64x2_32768": ("f24bafa159091945", 208142336 + 7953152),
-    "mxfp8_8192x65536": ("f24bafa159091945", 81149440 + 2087088128),
-    "mxfp4_8192x65536": ("f24bafa159091945", 42714368 + 2086714880),
-    "mxfp4_irregular_8192x65536": ("f24bafa159091945", 43566848 + 2086211328),
-    "thd_bf16_3seq_8192x32768": ("f24bafa159091945", 144908800 + 1012556032),
+    "bf16_batched_causal_4096": ("b9ac376f7fef89a9", 137480960 + 79439872),
+    "fp8_per_token_2048x32768": ("b9ac376f7fef89a9", 21690112 + 207621120),
+    "mxfp8_2048x32768": ("b9ac376f7fef89a9", 22220544 + 207505664),
+    "mxfp4_2048x32768": ("b9ac376f7fef89a9", 11735040 + 207220736),
+    "paged_fp8_decode_64x2_32768": ("b9ac376f7fef89a9", 208141568 + 7877120),
+    "mxfp8_8192x65536": ("b9ac376f7fef89a9", 80191232 + 2086541312),
+    "mxfp4_8192x65536": ("b9ac376f7fef89a9", 42626304 + 2086549248),
+    "mxfp4_irregular_8192x65536": ("b9ac376f7fef89a9", 44206336 + 2086041600),
+    "thd_bf16_3seq_8192x32768": ("b9ac376f7fef89a9", 144901888 + 1012543232),
 }
 
 
