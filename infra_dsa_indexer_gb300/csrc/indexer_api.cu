@@ -612,26 +612,34 @@ int indexer_topk(const void* logits, int logits_bf16, int64_t rows, int32_t N,
     sms = di->sm_count;
   }
   // One CTA per row; rows that cannot fill the GPU at 512 threads and four
-  // CTAs per SM get 1024 threads each.
-  const dim3 grid(static_cast<unsigned>(rows));
+  // CTAs per SM get 1024 threads each. Launched as a programmatic dependent
+  // of the previous kernel on the stream (the kernel waits for it first), so
+  // its launch overlaps that kernel's end instead of following it.
   const bool few = rows <= 2LL * sms;
   constexpr int kMany = dsa::kTopkThreads, kFew = dsa::kTopkThreadsFew;
-  if (logits_bf16) {
-    if (few)
-      dsa::topk_rows_kernel<kFew, true><<<grid, kFew, 0, stream>>>(logits, row_stride, N, k, idx,
-                                                                  idx_stride);
-    else
-      dsa::topk_rows_kernel<kMany, true><<<grid, kMany, 0, stream>>>(logits, row_stride, N, k,
-                                                                    idx, idx_stride);
-  } else {
-    if (few)
-      dsa::topk_rows_kernel<kFew, false><<<grid, kFew, 0, stream>>>(logits, row_stride, N, k,
-                                                                   idx, idx_stride);
-    else
-      dsa::topk_rows_kernel<kMany, false><<<grid, kMany, 0, stream>>>(logits, row_stride, N, k,
-                                                                     idx, idx_stride);
-  }
-  return cudaGetLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(rows));
+  cfg.blockDim = dim3(few ? kFew : kMany);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int n32 = static_cast<int>(N), k32 = static_cast<int>(k);
+  cudaError_t e;
+  if (logits_bf16)
+    e = few ? cudaLaunchKernelEx(&cfg, dsa::topk_rows_kernel<kFew, true>, logits, row_stride, n32,
+                                 k32, idx, idx_stride)
+            : cudaLaunchKernelEx(&cfg, dsa::topk_rows_kernel<kMany, true>, logits, row_stride,
+                                 n32, k32, idx, idx_stride);
+  else
+    e = few ? cudaLaunchKernelEx(&cfg, dsa::topk_rows_kernel<kFew, false>, logits, row_stride,
+                                 n32, k32, idx, idx_stride)
+            : cudaLaunchKernelEx(&cfg, dsa::topk_rows_kernel<kMany, false>, logits, row_stride,
+                                 n32, k32, idx, idx_stride);
+  return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -517,11 +517,17 @@ __device__ void topk_row(TopkShared& sh, const Src& src, int k, TopkOut o) {
 // per SM: the shared-memory phases of one row overlap the sweeps of the
 // others. With too few rows to fill the GPU (decode), 1024 threads per row
 // shorten each row's sweeps and shared-memory passes instead.
+//
+// Launched as a programmatic dependent of the kernel before it on the stream
+// (typically the logits kernel): its blocks may be placed while that kernel
+// finishes, and wait here until it has completed and its writes are visible
+// (a no-op when launched without the attribute).
 template <int NT, bool BF16_IN>
 __global__ void __launch_bounds__(NT, 2048 / NT)
     topk_rows_kernel(const void* __restrict__ logits, int64_t row_stride, int N, int k,
                      int32_t* __restrict__ idx, int64_t idx_stride) {
   __shared__ TopkShared sh;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t row = blockIdx.x;
   const DenseRow<BF16_IN> src{
       reinterpret_cast<const char*>(logits) + row * row_stride * (BF16_IN ? 2 : 4), N};
