@@ -30,7 +30,7 @@ def _paged_and_contiguous(case):
     return tp["out"], tc["out"]
 
 
-@pytest.mark.parametrize("page_size", [64, 128, 192, 256, 320])
+@pytest.mark.parametrize("page_size", [64, 128, 192, 256, 320, 1024])
 @pytest.mark.parametrize("fmt", ALL)
 def test_paged_equals_contiguous_and_oracle(fmt, page_size):
     case = synth.make_case(fmt, 3, 12, 1000, seed=140 + fmt, windows="irregular",
