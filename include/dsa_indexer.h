@@ -235,6 +235,10 @@ IDX_API int indexer_paged_logits(const void* q, const uint8_t* q_sf, const void*
  *  k            1 <= k.
  *  idx          device, [rows, idx_stride] int32, idx_stride >= k; written in
  *               columns [0, k) of every row.
+ * Stream-ordered like every call: the selection kernel is launched as a
+ * programmatic dependent of the previous kernel on `stream`, so it may be
+ * placed on the GPU while that kernel finishes, but it reads the logits only
+ * after that kernel has completed.
  * Returns IDX_OK once enqueued; IDX_ERR_NULL, IDX_ERR_SHAPE, IDX_ERR_ALIGN,
  * IDX_ERR_DEVICE, IDX_ERR_CUDA as for indexer_logits. */
 IDX_API int indexer_topk(const void* logits, int logits_bf16, int64_t rows, int32_t N,
