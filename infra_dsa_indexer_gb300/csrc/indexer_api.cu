@@ -164,6 +164,27 @@ int encode_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, in
   return r == CUDA_SUCCESS ? IDX_OK : IDX_ERR_CUDA;
 }
 
+// Launches a selection kernel (it starts with griddepcontrol.wait) as a
+// programmatic dependent of the previous kernel on the stream: its blocks may
+// be placed while that kernel finishes, and read its output only after it
+// has completed.
+template <typename... KArgs, typename... Args>
+int launch_dependent(void (*kernel)(KArgs...), unsigned grid, unsigned block, cudaStream_t stream,
+                     Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+  return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+}
+
 template <int FMT, bool NEG_EPI, bool OUT_BF16, bool PAGED, int MODE = dsa::kModeLogits,
           int RB = dsa::kRowsPerBlock, bool SF_KEYS = false>
 int launch_kernel(const KernelParams& prm, int grid, DeviceInfo* di, cudaStream_t stream) {
@@ -617,29 +638,16 @@ int indexer_topk(const void* logits, int logits_bf16, int64_t rows, int32_t N,
   // its launch overlaps that kernel's end instead of following it.
   const bool few = rows <= 2LL * sms;
   constexpr int kMany = dsa::kTopkThreads, kFew = dsa::kTopkThreadsFew;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(rows));
-  cfg.blockDim = dim3(few ? kFew : kMany);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const int n32 = static_cast<int>(N), k32 = static_cast<int>(k);
-  cudaError_t e;
+  const unsigned grid = static_cast<unsigned>(rows);
   if (logits_bf16)
-    e = few ? cudaLaunchKernelEx(&cfg, dsa::topk_rows_kernel<kFew, true>, logits, row_stride, n32,
-                                 k32, idx, idx_stride)
-            : cudaLaunchKernelEx(&cfg, dsa::topk_rows_kernel<kMany, true>, logits, row_stride,
-                                 n32, k32, idx, idx_stride);
-  else
-    e = few ? cudaLaunchKernelEx(&cfg, dsa::topk_rows_kernel<kFew, false>, logits, row_stride,
-                                 n32, k32, idx, idx_stride)
-            : cudaLaunchKernelEx(&cfg, dsa::topk_rows_kernel<kMany, false>, logits, row_stride,
-                                 n32, k32, idx, idx_stride);
-  return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+    return few ? launch_dependent(dsa::topk_rows_kernel<kFew, true>, grid, kFew, stream, logits,
+                                  row_stride, N, k, idx, idx_stride)
+               : launch_dependent(dsa::topk_rows_kernel<kMany, true>, grid, kMany, stream, logits,
+                                  row_stride, N, k, idx, idx_stride);
+  return few ? launch_dependent(dsa::topk_rows_kernel<kFew, false>, grid, kFew, stream, logits,
+                                row_stride, N, k, idx, idx_stride)
+             : launch_dependent(dsa::topk_rows_kernel<kMany, false>, grid, kMany, stream, logits,
+                                row_stride, N, k, idx, idx_stride);
 }
 
 }  // extern "C"
@@ -714,6 +722,11 @@ int indexer_logits_topk(const void* q, const uint8_t* q_sf, const void* k, const
     if (st) return st;
     sms = di->sm_count;
   }
+  // The filter pass's mask words start at zero (cleared first, so that the
+  // threshold and merge kernels directly follow the logits passes they read
+  // and are launched as their programmatic dependents).
+  if (cudaMemsetAsync(mask, 0, 4 * ws.mask_stride * ws.rows, stream) != cudaSuccess)
+    return IDX_ERR_CUDA;
   // 1. the sample pass: every kSampleEvery-th key tile, compact FP32 rows
   PassArgs pass;
   pass.mode = dsa::kModeSample;
@@ -721,19 +734,16 @@ int indexer_logits_topk(const void* q, const uint8_t* q_sf, const void* k, const
   int st = enqueue_logits(q, q_sf, k, k_sf, k_scales, w, ks, ke, sm_scale, 1, smp, shape, stream,
                           false, nullptr, pass);
   if (st) return st;
-  if (cudaMemsetAsync(mask, 0, 4 * ws.mask_stride * ws.rows, stream) != cudaSuccess)
-    return IDX_ERR_CUDA;
   // 2. each row's threshold: the topk-th largest of its sample
-  const dim3 grid(static_cast<unsigned>(ws.rows));
+  const unsigned grid = static_cast<unsigned>(ws.rows);
   const bool few = ws.rows <= 2LL * sms;
   constexpr int kMany = dsa::kTopkThreads, kFew = dsa::kTopkThreadsFew;
-  if (few)
-    dsa::topk_threshold_kernel<kFew><<<grid, kFew, 0, stream>>>(smp, ws.ns_cols,
-                                                              static_cast<int>(ws.ns_cols), topk, thr);
-  else
-    dsa::topk_threshold_kernel<kMany><<<grid, kMany, 0, stream>>>(smp, ws.ns_cols,
-                                                                static_cast<int>(ws.ns_cols), topk, thr);
-  if (cudaGetLastError() != cudaSuccess) return IDX_ERR_CUDA;
+  const int ns = static_cast<int>(ws.ns_cols);
+  st = few ? launch_dependent(dsa::topk_threshold_kernel<kFew>, grid, kFew, stream, smp,
+                              ws.ns_cols, ns, topk, thr)
+           : launch_dependent(dsa::topk_threshold_kernel<kMany>, grid, kMany, stream, smp,
+                              ws.ns_cols, ns, topk, thr);
+  if (st) return st;
   // 3. the other key tiles: append the values at or above the threshold
   pass.mode = dsa::kModeFilter;
   pass.out_row_stride = ws.cap;
@@ -745,15 +755,12 @@ int indexer_logits_topk(const void* q, const uint8_t* q_sf, const void* k, const
                            false, nullptr, pass)))
     return st;
   // 4. the top-k of sample and candidates
-  if (few)
-    dsa::topk_merge_kernel<kFew><<<grid, kFew, 0, stream>>>(
-        smp, ws.ns_cols, static_cast<int>(ws.ns_cols), kept, ws.cap, mask, ws.mask_stride,
-        dsa::kSampleEvery, topk, idx, idx_stride);
-  else
-    dsa::topk_merge_kernel<kMany><<<grid, kMany, 0, stream>>>(
-        smp, ws.ns_cols, static_cast<int>(ws.ns_cols), kept, ws.cap, mask, ws.mask_stride,
-        dsa::kSampleEvery, topk, idx, idx_stride);
-  return cudaGetLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+  return few ? launch_dependent(dsa::topk_merge_kernel<kFew>, grid, kFew, stream, smp, ws.ns_cols,
+                                ns, kept, ws.cap, mask, ws.mask_stride, dsa::kSampleEvery, topk,
+                                idx, idx_stride)
+             : launch_dependent(dsa::topk_merge_kernel<kMany>, grid, kMany, stream, smp,
+                                ws.ns_cols, ns, kept, ws.cap, mask, ws.mask_stride,
+                                dsa::kSampleEvery, topk, idx, idx_stride);
 }
 
 int indexer_thd_windows(const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,

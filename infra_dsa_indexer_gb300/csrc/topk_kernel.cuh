@@ -542,6 +542,7 @@ __global__ void __launch_bounds__(NT, 2048 / NT)
     topk_threshold_kernel(const float* __restrict__ s, int64_t s_stride, int ns, int k,
                           float* __restrict__ thr) {
   __shared__ TopkShared sh;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // see topk_rows_kernel
   const int64_t row = blockIdx.x;
   const DenseRow<false> src{reinterpret_cast<const char*>(s + row * s_stride), ns};
   topk_row<NT>(sh, src, k, TopkOut{nullptr, thr + row});
@@ -557,6 +558,7 @@ __global__ void __launch_bounds__(NT, 2048 / NT)
                       const uint32_t* __restrict__ mask, int64_t mask_stride, int sample_every,
                       int k, int32_t* __restrict__ idx, int64_t idx_stride) {
   __shared__ TopkShared sh;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // see topk_rows_kernel
   const int64_t row = blockIdx.x;
   const int ngroups = static_cast<int>(mask_stride);
   const MergeRow src{s + row * s_stride, ns, kept + row * kept_stride, mask + row * mask_stride,
