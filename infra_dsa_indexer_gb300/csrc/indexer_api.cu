@@ -463,14 +463,16 @@ int enqueue_logits(const void* q, const uint8_t* q_sf, const void* k, const uint
   // row-block is taken as tiles_max tiles (the host does not read windows),
   // so fewer pieces than nchunk are taken only while the grid still runs at
   // least 16 rounds (unit sizes vary; a short grid's tail does not follow
-  // the estimate). Measured: 2048 x 32768 calls (2048 units in 13.5 rounds
+  // the estimate), or when they fit the whole grid in one round (the
+  // 128 x 1024 causal call: 128 two-tile units, 14.5 -> 12.5 µs, against 256
+  // one-tile units in two rounds). Measured: 2048 x 32768 calls (2048 units in 13.5 rounds
   // at 4 pieces) take 5 pieces and run 2% faster; 8192 x 65536 calls take 4
   // instead of 8 (-0.4%).
   {
     int64_t best = nchunk, best_cost = INT64_MAX;
     for (int64_t n = (nchunk + 1) / 2; n <= std::min<int64_t>(2 * nchunk, tiles_max); ++n) {
       const int64_t rounds = (row_blocks * n + di->sm_count - 1) / di->sm_count;
-      if (n < nchunk && rounds < 16) continue;
+      if (n < nchunk && rounds < 16 && rounds > 1) continue;
       const int64_t cost = rounds * ((tiles_max + n - 1) / n + 2);
       if (cost < best_cost) {
         best = n;
